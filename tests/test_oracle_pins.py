@@ -1,0 +1,347 @@
+"""Pins of the CPU oracle to things other than itself (no GPU).
+
+Each test checks the oracle against a closed form, a brute-force restatement
+written independently here (pure Python, fp64 where it is arithmetic), an
+invariant of the layer, or a value printed on the pages (tests/golden/).
+"""
+import math
+import os
+import struct
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import GOLDEN
+
+F32 = np.float32
+
+
+# ---------------------------------------------------------------------------
+# helpers written independently of the oracle
+# ---------------------------------------------------------------------------
+
+def bf16_bits_to_float(bits: int) -> float:
+    return struct.unpack(">f", struct.pack(">I", (int(bits) & 0xFFFF) << 16))[0]
+
+
+def brute_dequant_row(words_row, scales_row):
+    """Pure-Python dequantisation of one row: list of floats."""
+    out = []
+    for c, w in enumerate(words_row):
+        u = int(w) & 0xFFFFFFFF
+        for j in range(8):
+            q = ((u >> (4 * j)) & 0xF) - 8
+            out.append(q * bf16_bits_to_float(scales_row[(8 * c + j) // 32]))
+    return out
+
+
+def brute_expert(x, w13, s13, w2, s2):
+    """fp64 pure-Python gated-SiLU expert on one token."""
+    I = len(w2[0]) * 8
+    W13 = [brute_dequant_row(w13[n], s13[n]) for n in range(2 * I)]
+    gu = [sum(a * b for a, b in zip(row, x)) for row in W13]
+    h = [gu[i] / (1.0 + math.exp(-gu[i])) * gu[I + i] for i in range(I)]
+    W2 = [brute_dequant_row(w2[n], s2[n]) for n in range(len(w2))]
+    return [sum(a * b for a, b in zip(row, h)) for row in W2]
+
+
+def rand_layer(E, H, I, seed, lo=0.005, hi=0.02):
+    import synth
+    return synth.make_layer(synth.LayerShape(E=E, top_k=1, H=H, I=I), seed=seed, scale_lo=lo, scale_hi=hi)
+
+
+def ulp32(v):
+    v = np.abs(np.asarray(v, dtype=np.float32))
+    return (np.nextafter(v, F32(np.inf)) - v).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# weight format
+# ---------------------------------------------------------------------------
+
+def read_nibble_fixture():
+    rows = []
+    with open(os.path.join(GOLDEN, "nibble_layout.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            parts = line.split()
+            q = [int(v) for v in parts[:8]]
+            word = np.array([int(parts[8], 16)], dtype=np.uint32).view(np.int32)[0]
+            rows.append((q, word))
+    return rows
+
+
+def test_nibble_layout_worked_examples():
+    for q, word in read_nibble_fixture():
+        assert oracle.pack_int4(np.array([q]))[0, 0] == word
+        assert list(oracle.unpack_int4(np.array([[word]], dtype=np.int32))[0]) == q
+
+
+def test_pack_unpack_round_trip():
+    rng = np.random.default_rng(3)
+    q = rng.integers(-8, 8, size=(37, 96))
+    assert np.array_equal(oracle.unpack_int4(oracle.pack_int4(q)), q)
+    words = rng.integers(-2**31, 2**31, size=(5, 12), dtype=np.int64).astype(np.int32)
+    assert np.array_equal(oracle.pack_int4(oracle.unpack_int4(words)), words)
+
+
+def test_dequant_matches_brute_force():
+    layer = rand_layer(1, 64, 32, seed=5)
+    W = oracle.dequant(layer["w2"][0], layer["s2"][0])
+    for n in (0, 7, 63):
+        ref = brute_dequant_row(layer["w2"][0][n], layer["s2"][0][n])
+        assert np.array_equal(W[n], np.array(ref, dtype=np.float32))   # exact products
+
+
+def test_param_count_identity():
+    """Three H x I int4 matrices per expert reproduce the page's int32-stored count."""
+    vals = {}
+    with open(os.path.join(GOLDEN, "kimi_k26_param_counts.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = int(v)
+    per_expert = oracle.expert_int4_params(vals["hidden"], vals["moe_intermediate"])
+    assert vals["moe_layers"] * vals["routed_experts"] * per_expert == vals["int32_stored_params"]
+    # and the oracle's tensor shapes carry exactly that many int4 values
+    layer = rand_layer(2, 64, 32, seed=1)
+    n = layer["w13"][0].size * 8 + layer["w2"][0].size * 8
+    assert n == oracle.expert_int4_params(64, 32)
+
+
+# ---------------------------------------------------------------------------
+# defined sigmoid
+# ---------------------------------------------------------------------------
+
+def test_sigmoid_special_values():
+    s = oracle.sigmoid_def(np.array([0.0, -0.0, np.inf, -np.inf], dtype=np.float32))
+    assert s[0] == F32(0.5) and s[1] == F32(0.5)
+    assert s[2] == F32(1.0) and s[3] == F32(0.0)
+    assert np.isnan(oracle.sigmoid_def(np.float32(np.nan)))
+    assert oracle.exp_def(np.float32(0.0)) == F32(1.0)
+    assert oracle.exp_def(np.float32(1.0)) == F32(math.e)      # within rounding: e rounds to the fp32 of e
+
+
+def test_sigmoid_within_ulp_of_fp64():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([np.linspace(-100, 100, 2_000_001, dtype=np.float32),
+                        (rng.standard_normal(1_000_000) * 10).astype(np.float32),
+                        (rng.standard_normal(200_000) * 1e-3).astype(np.float32)])
+    s = oracle.sigmoid_def(x).astype(np.float64)
+    ref = 1.0 / (1.0 + np.exp(-x.astype(np.float64)))
+    keep = ref > 1e-37                               # fp32 normal range
+    err = np.abs(s - ref)[keep] / ulp32(ref[keep])
+    assert err.max() <= 3.0, err.max()
+    t = np.linspace(-87, 88, 500_001, dtype=np.float32)
+    e = oracle.exp_def(t).astype(np.float64)
+    ref_e = np.exp(t.astype(np.float64))
+    assert (np.abs(e - ref_e) / ulp32(ref_e)).max() <= 1.5
+
+
+def test_sigmoid_monotone_and_symmetric():
+    x = np.sort(np.random.default_rng(1).standard_normal(400_000).astype(np.float32) * 20)
+    s = oracle.sigmoid_def(x)
+    assert np.all(np.diff(s) >= 0)
+    sym = s.astype(np.float64) + oracle.sigmoid_def(-x).astype(np.float64)
+    assert np.abs(sym - 1.0).max() <= 4 * 2.0 ** -24
+
+
+# ---------------------------------------------------------------------------
+# routing
+# ---------------------------------------------------------------------------
+
+def brute_topk(scores_row, k):
+    """Rank by counting how many experts beat each one (O(E^2), pure Python)."""
+    E = len(scores_row)
+    key = [(-1.0 if math.isnan(v) else float(v)) for v in scores_row]
+    rank = []
+    for e in range(E):
+        beaten_by = sum(1 for f in range(E) if key[f] > key[e] or (key[f] == key[e] and f < e))
+        rank.append(beaten_by)
+    ids = [None] * E
+    for e, r in enumerate(rank):
+        ids[r] = e
+    return ids[:k]
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (33, 5), (16, 16), (1, 1)])
+def test_topk_matches_brute_force(E, k):
+    rng = np.random.default_rng(E * 100 + k)
+    logits = rng.standard_normal((40, E)).astype(np.float32)
+    logits[0, :] = 0.0                                     # all tied
+    if E >= 4:
+        logits[1, :4] = [20.0, 25.0, 17.0, 30.0]           # distinct logits, equal fp32 scores
+        logits[2, ::2] = np.inf
+        logits[3, 1::2] = -np.inf
+        logits[4, :] = np.float32(1.5)
+    ids, w, s = oracle.route(logits, k)
+    for t in range(logits.shape[0]):
+        assert list(ids[t]) == brute_topk(s[t], k), t
+
+
+def test_crafted_tie_goes_to_lowest_index():
+    logits = np.full((1, 6), -3.0, dtype=np.float32)
+    logits[0, [1, 2, 4]] = [20.0, 25.0, 30.0]             # sigmoid of each rounds to 1.0f
+    ids, w, s = oracle.route(logits, 2)
+    assert s[0, 1] == s[0, 2] == s[0, 4] == F32(1.0)
+    assert list(ids[0]) == [1, 2]
+    assert w[0, 0] == w[0, 1] == F32(0.5)
+
+
+def test_weights_sum_to_one():
+    rng = np.random.default_rng(7)
+    for E, k in [(384, 8), (8, 2), (64, 6)]:
+        logits = (rng.standard_normal((200, E)) * 4).astype(np.float32)
+        _, w, _ = oracle.route(logits, k)
+        assert np.abs(w.astype(np.float64).sum(1) - 1.0).max() <= k * 2.0 ** -24
+
+
+def test_weights_when_every_score_underflows():
+    logits = np.full((2, 5), -100.0, dtype=np.float32)
+    ids, w, s = oracle.route(logits, 3)
+    assert np.all(s == 0)
+    assert list(ids[0]) == [0, 1, 2]
+    assert np.all(w == F32(1.0) / F32(3))
+
+
+def test_renormalisation_matches_fp64_within_rounding():
+    rng = np.random.default_rng(11)
+    logits = rng.standard_normal((50, 32)).astype(np.float32)
+    ids, w, s = oracle.route(logits, 4)
+    for t in range(50):
+        sel = [float(s[t, e]) for e in ids[t]]
+        tot = sum(sel)
+        for j in range(4):
+            assert abs(float(w[t, j]) - sel[j] / tot) <= 3 * 2.0 ** -24
+
+
+# ---------------------------------------------------------------------------
+# permutation
+# ---------------------------------------------------------------------------
+
+def brute_permute(ids, E):
+    T, k = ids.shape
+    rows = []
+    for e in range(E):
+        for t in range(T):
+            for j in range(k):
+                if ids[t, j] == e:
+                    rows.append((t, j))
+    counts = [sum(1 for (t, j) in rows if ids[t, j] == e) for e in range(E)]
+    offsets = [0]
+    for c in counts:
+        offsets.append(offsets[-1] + c)
+    inv = [0] * (T * k)
+    for p, (t, j) in enumerate(rows):
+        inv[t * k + j] = p
+    return offsets, [t for (t, j) in rows], inv
+
+
+@pytest.mark.parametrize("T,E,k", [(16, 8, 2), (37, 33, 5), (5, 1, 1), (64, 12, 12)])
+def test_permute_matches_brute_force(T, E, k):
+    rng = np.random.default_rng(T + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    ids, _, _ = oracle.route(logits, k)
+    off, srt, inv = oracle.permute(ids, E)
+    b_off, b_srt, b_inv = brute_permute(ids, E)
+    assert list(off) == b_off and list(srt) == b_srt and list(inv) == b_inv
+
+
+# ---------------------------------------------------------------------------
+# expert MLP, combine, layer
+# ---------------------------------------------------------------------------
+
+def test_single_expert_top1_equals_dense_brute_force():
+    import synth
+    layer = rand_layer(1, 64, 32, seed=9)
+    x_bits, logits = synth.make_tokens(3, 64, 1, seed=4)
+    res = oracle.moe_layer(x_bits, logits, layer, k=1)
+    assert np.all(res["weights"] == F32(1.0))
+    for t in range(3):
+        x = [bf16_bits_to_float(b) for b in x_bits[t]]
+        ref = np.array(brute_expert(x, layer["w13"][0], layer["s13"][0], layer["w2"][0], layer["s2"][0]))
+        got = res["out"][t].astype(np.float64)
+        rms = np.sqrt(np.mean(ref ** 2))
+        assert np.abs(got - ref).max() <= 1e-5 * rms + 1e-12
+
+
+def test_gate_and_up_are_not_interchangeable():
+    """Swapping the gate and up halves changes the output (pins which half is the gate)."""
+    layer = rand_layer(1, 64, 32, seed=2)
+    x = oracle.bf16_to_f32(np.random.default_rng(0).integers(0x3000, 0x4000, 64).astype(np.uint16))
+    y = oracle.expert_mlp(x, layer["w13"][0], layer["s13"][0], layer["w2"][0], layer["s2"][0])
+    sw = np.concatenate([layer["w13"][0][32:], layer["w13"][0][:32]])
+    ss = np.concatenate([layer["s13"][0][32:], layer["s13"][0][:32]])
+    y2 = oracle.expert_mlp(x, sw, ss, layer["w2"][0], layer["s2"][0])
+    assert not np.allclose(y, y2, rtol=1e-3)
+    xs = [float(v) for v in x]
+    ref = np.array(brute_expert(xs, layer["w13"][0], layer["s13"][0], layer["w2"][0], layer["s2"][0]))
+    assert np.abs(y - ref).max() <= 1e-5 * np.sqrt(np.mean(ref ** 2))
+
+
+def test_identical_experts_give_the_single_expert_output():
+    import synth
+    one = rand_layer(1, 64, 32, seed=12)
+    layer = {key: np.repeat(v, 4, axis=0) for key, v in one.items()}
+    x_bits, logits = synth.make_tokens(6, 64, 4, seed=8)
+    res = oracle.moe_layer(x_bits, logits, layer, k=3)
+    for t in range(6):
+        y = oracle.expert_mlp(oracle.bf16_to_f32(x_bits[t]), one["w13"][0], one["s13"][0], one["w2"][0], one["s2"][0])
+        assert np.abs(res["out"][t] - y).max() <= 4 * 2.0 ** -24 * np.abs(y).max()
+
+
+def test_power_of_two_scale_doubles_exactly():
+    layer = rand_layer(1, 64, 32, seed=13)
+    x = oracle.bf16_to_f32(np.random.default_rng(1).integers(0x3000, 0x4000, 64).astype(np.uint16))
+    y = oracle.expert_mlp(x, layer["w13"][0], layer["s13"][0], layer["w2"][0], layer["s2"][0])
+    s2 = (oracle.bf16_to_f32(layer["s2"][0]) * 2).view(np.uint32) >> np.uint32(16)
+    y2 = oracle.expert_mlp(x, layer["w13"][0], layer["s13"][0], layer["w2"][0], s2.astype(np.uint16))
+    assert np.array_equal(y2, 2 * y)
+    s13 = layer["s13"][0].copy()                      # double the up half only
+    s13[32:] = ((oracle.bf16_to_f32(s13[32:]) * 2).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    y3 = oracle.expert_mlp(x, layer["w13"][0], s13, layer["w2"][0], layer["s2"][0])
+    assert np.array_equal(y3, 2 * y)
+
+
+def test_zero_weights_give_exact_zero_and_shared_only():
+    import synth
+    E, H, I = 3, 64, 32
+    layer = rand_layer(E, H, I, seed=4)
+    layer["w13"][:] = np.int32(np.uint32(0x88888888).view(np.int32))
+    layer["w2"][:] = np.int32(np.uint32(0x88888888).view(np.int32))
+    x_bits, logits = synth.make_tokens(4, H, E, seed=2)
+    res = oracle.moe_layer(x_bits, logits, layer, k=2)
+    assert np.all(res["out"] == 0)
+    layer["sh_gu"] = synth.normal_bf16((2 * 32, H), 0.02, 0, 4)
+    layer["sh_d"] = synth.normal_bf16((H, 32), 0.02, 0, 5)
+    res = oracle.moe_layer(x_bits, logits, layer, k=2, with_shared=True)
+    for t in range(4):
+        x = [bf16_bits_to_float(b) for b in x_bits[t]]
+        Wg = [[bf16_bits_to_float(b) for b in row] for row in layer["sh_gu"]]
+        Wd = [[bf16_bits_to_float(b) for b in row] for row in layer["sh_d"]]
+        gu = [sum(a * b for a, b in zip(r, x)) for r in Wg]
+        h = [gu[i] / (1 + math.exp(-gu[i])) * gu[32 + i] for i in range(32)]
+        ref = np.array([sum(a * b for a, b in zip(r, h)) for r in Wd])
+        assert np.abs(res["out"][t] - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_combine_weighted_rank_order_sum():
+    rng = np.random.default_rng(5)
+    T, k, E, H = 7, 3, 5, 16
+    ids, w, _ = oracle.route(rng.standard_normal((T, E)).astype(np.float32), k)
+    off, srt, inv = oracle.permute(ids, E)
+    y = rng.standard_normal((T * k, H)).astype(np.float32)
+    out = oracle.combine(y, inv, w)
+    for t in range(T):
+        ref = [sum(float(w[t, j]) * float(y[inv[t * k + j], c]) for j in range(k)) for c in range(H)]
+        assert np.abs(out[t] - np.array(ref)).max() <= 1e-6 * max(1.0, np.abs(ref).max())
+    # the row of assignment (t, j) holds that token
+    assert np.all(srt[inv] == np.repeat(np.arange(T), k))
+
+
+def test_rmsnorm_unit_rms():
+    x = np.random.default_rng(0).standard_normal((4, 256)).astype(np.float32) * 7
+    n = oracle.rmsnorm(x)
+    assert np.abs(np.sqrt(np.mean(n.astype(np.float64) ** 2, axis=1)) - 1).max() < 1e-5
