@@ -1,0 +1,452 @@
+"""Benchmark of the routed-expert W4A16 MoE layer on GB300.
+
+One step = one pass of the whole layer (route, permute + gather, gate/up
+grouped GEMM with SiLU*up, down grouped GEMM, combine) over one batch of the
+workload, through the C ABI (moe_forward). Default workload: the full-size
+decode layer (384 experts, top-8, hidden 7168, intermediate 2048, int4 group
+32, T = 64 tokens), seeded synthetic inputs. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica of the workload
+on its own GPU (the layer has no cross-token exchange); value = tokens of all
+ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill TFLOPS as % of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+WORKLOADS = {
+    "decode_t64": dict(shape=synth.FULL, T=64, skew=None),
+    "prefill_t4096_zipf": dict(shape=synth.FULL, T=4096, skew=1.1),
+    "tiny": dict(shape=synth.TINY, T=16, skew=None),
+    "decode_t1_shared": dict(shape=synth.FULL_WITH_SHARED, T=1, skew=None),
+    "decode_t8_shared": dict(shape=synth.FULL_WITH_SHARED, T=8, skew=None),
+    "decode_t32_shared": dict(shape=synth.FULL_WITH_SHARED, T=32, skew=None),
+    "decode_t128_shared": dict(shape=synth.FULL_WITH_SHARED, T=128, skew=None),
+    "decode_t512_shared": dict(shape=synth.FULL_WITH_SHARED, T=512, skew=None),
+}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), \
+            "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def workload_desc(name, w):
+    s = w["shape"]
+    txt = (f"{name}: routed MoE layer E={s.E} top-{s.top_k} H={s.H} I={s.I}, int4 group-32 weights + bf16 "
+           f"scales, bf16 activations, T={w['T']} tokens")
+    if s.shared_I:
+        txt += f", + bf16 shared expert I={s.shared_I}"
+    if w["skew"]:
+        txt += f", router logits N(0,1) + Zipf(s={w['skew']}) expert-popularity bias"
+    else:
+        txt += ", router logits N(0,1)"
+    return txt
+
+
+def make_inputs(w, seed=0):
+    s = w["shape"]
+    arrays = synth.make_layer(s, seed=seed)
+    bias = synth.zipf_bias(s.E, w["T"], s.top_k, w["skew"], seed) if w["skew"] else None
+    x, logits = synth.make_tokens(w["T"], s.H, s.E, seed=seed, bias=bias)
+    return arrays, x, logits
+
+
+def expert_bytes(s):
+    """int4 words + bf16 scales of one routed expert (gate/up, down)."""
+    gu = 2 * s.I * s.H // 2 + 2 * s.I * (s.H // 32) * 2
+    dn = s.H * s.I // 2 + s.H * (s.I // 32) * 2
+    return gu, dn
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling around the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def profile_traffic(kernel_tag: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_sha and m_b):
+        return None
+    if m_sha.group(1) != kernel_source_sha():
+        return None
+    return float(m_b.group(1))
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "w4a16_mixture_experts_sigmoid_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (only bench's cpu_baseline leg and --impl reference use the oracle)
+# ---------------------------------------------------------------------------
+
+def _oracle_tokens_per_s(w, budget_s: float, seed=0):
+    import oracle
+    arrays, x, logits = make_inputs(w, seed)
+    s = w["shape"]
+    order = np.random.default_rng(0).permutation(w["T"])
+    done = []
+    t0 = time.perf_counter()
+    for t in order:
+        oracle.moe_layer(x, logits, arrays, s.top_k, tokens=[int(t)], with_shared=bool(s.shared_I))
+        done.append(int(t))
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return len(done) / el, done, el
+
+
+def cpu_baseline(workload: str, budget_s: float = 12.0):
+    """Run the oracle in a fresh interpreter with its BLAS threads pinned to the host's core count."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"v, done, el = bench._oracle_tokens_per_s(bench.WORKLOADS[{workload!r}], {budget_s}); "
+            f"print(json.dumps({{'v': v, 'done': done, 'el': el}}))")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"failed: {r.stderr.strip()[-300:]}"}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": res["v"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{len(res['done'])} of the {WORKLOADS[workload]['T']} tokens of {workload} "
+                       f"(seeded order), each a full layer output (routing + {WORKLOADS[workload]['shape'].top_k} "
+                       f"experts dequantised in fp32 + combine), {res['el']:.1f} s of CPU work, numpy/BLAS "
+                       f"threads = {cores}")}
+
+
+# ---------------------------------------------------------------------------
+# the arms
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """The oracle as the reference arm: one step = one (token, expert) pair of the workload."""
+    ws, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    import oracle
+    w = WORKLOADS[args.workload]
+    s = w["shape"]
+    arrays, x, logits = make_inputs(w)
+    ids, rw, _ = oracle.route(logits, s.top_k)
+    units = [(t, j) for t in range(w["T"]) for j in range(s.top_k)]
+
+    def step(i):
+        t, j = units[i % len(units)]
+        xf = oracle.bf16_to_f32(x[t])
+        e = int(ids[t, j])
+        y = oracle.expert_mlp(xf, arrays["w13"][e], arrays["s13"][e], arrays["w2"][e], arrays["s2"][e])
+        return rw[t, j] * y
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = (args.steps / s.top_k) / el
+    cores = os.cpu_count() or 1
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, w), "T": w["T"], "E": s.E, "top_k": s.top_k,
+                   "H": s.H, "I": s.I},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"one (token, expert) pair per step, {args.steps} pairs = "
+                                   f"{args.steps / s.top_k:.2f} tokens of {args.workload}; BLAS threads default"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    s = w["shape"]
+    T = w["T"]
+    arrays, x, logits = make_inputs(w, seed=0)
+    layer = MoeW4A16Layer.from_arrays(s, arrays, device=dev)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    ld = torch.from_numpy(logits).to(dev)
+    out = torch.empty((T, s.H), dtype=torch.int16, device=dev)
+    flags = args.flags
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.forward(xd, ld, out=out, flags=flags)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = layer.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {B.moe_status_string(st)}")
+
+    # touched experts of this batch (routing is fixed across steps)
+    R = T * s.top_k
+    d_ids = torch.empty((T, s.top_k), dtype=torch.int32, device=dev)
+    d_w = torch.empty((T, s.top_k), dtype=torch.float32, device=dev)
+    d_off = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
+    d_srt = torch.empty(R, dtype=torch.int32, device=dev)
+    d_inv = torch.empty(R, dtype=torch.int32, device=dev)
+    xperm = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    h = torch.empty((R, s.I), dtype=torch.int16, device=dev)
+    y = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    wsp = layer.workspace(T)
+    B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
+    B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp)
+    torch.cuda.synchronize(dev)
+    counts = np.diff(d_off.cpu().numpy())
+    touched = int((counts > 0).sum())
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = B.moe_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = B.moe_launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    st = layer.check_status()
+    if st != 0:
+        raise RuntimeError(f"device status after the timed region: {B.moe_status_string(st)}")
+    value = T * world / (ms_max * 1e-3)
+
+    # per-kernel pass: the same kernels through the split entry points, events between them
+    ksteps = max(10, min(args.steps, 100))
+    names = ["route", "permute_gather", "gemm_gate_up", "gemm_down", "combine"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(ksteps)]
+    for i in range(ksteps):
+        E_ = ev[i]
+        E_[0].record(stream)
+        B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
+        E_[1].record(stream)
+        B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp)
+        E_[2].record(stream)
+        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp, flags)
+        E_[3].record(stream)
+        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags)
+        E_[4].record(stream)
+        B.moe_combine(y, d_inv, d_w, T, s.top_k, s.H, None, out)
+        E_[5].record(stream)
+    torch.cuda.synchronize(dev)
+    per = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(ksteps)) for j, n in
+           enumerate(names)}
+    gu_b, dn_b = expert_bytes(s)
+    alg = {
+        "gemm_gate_up": touched * gu_b + R * s.H * 2 + R * s.I * 2,
+        "gemm_down": touched * dn_b + R * s.I * 2 + R * s.H * 2,
+    }
+    flops = {"gemm_gate_up": 2.0 * R * s.H * 2 * s.I, "gemm_down": 2.0 * R * s.I * s.H}
+    dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: per[n])
+    hbm, bf16_burst, bf16_sus, src = load_peaks()
+    achieved = alg[dominant] / (per[dominant] * 1e-3) / 1e9
+    traffic = profile_traffic(dominant, args.workload)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "kernel": dominant, "kernel_ms": per[dominant],
+                "algorithmic_bytes_per_launch": alg[dominant], "peak_source": f"{src} hbm_gbs"}
+    step_bytes = touched * (gu_b + dn_b) + T * s.H * 2 * 2 + T * s.E * 4
+    if s.shared_I:
+        step_bytes += 3 * s.H * s.shared_I * 2
+    step_flops = 6.0 * T * s.top_k * s.H * s.I + (6.0 * T * s.H * s.shared_I)
+    t_hbm = step_bytes / (hbm * 1e9)
+    t_tc = step_flops / (bf16_sus * 1e12)
+    step_roof = {"touched_experts": touched, "bytes": step_bytes, "flops": step_flops,
+                 "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9, "tflops": step_flops / (ms * 1e-3) / 1e12,
+                 "roofline_ms": max(t_hbm, t_tc) * 1e3, "frac": max(t_hbm, t_tc) / (ms * 1e-3),
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "kernels_ms": per}
+
+    # end to end: host buffers in, host result out, copies inside the timed region
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    lh = torch.from_numpy(logits).pin_memory()
+    oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, lh, oh, flags=flags)
+    torch.cuda.synchronize(dev)
+    esteps = max(10, min(args.steps, 200))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(esteps):
+        layer.forward_host(xh, lh, oh, flags=flags)
+        torch.cuda.current_stream(dev).synchronize()
+    e2e_s = (time.perf_counter() - t0) / esteps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": x.nbytes + logits.nbytes,
+           "d2h_bytes_per_step": T * s.H * 2, "ms_per_step": e2e_s * 1e3,
+           "note": "moe_forward_host: pinned host x/logits -> device, layer, result -> pinned host, stream "
+                   "synchronised every step"}
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(args.workload) if (world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, w), "T": T, "E": s.E, "top_k": s.top_k, "H": s.H,
+                   "I": s.I, "shared_I": s.shared_I, "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: each step streams {touched} experts' int4 weights "
+                         f"({touched * (gu_b + dn_b) / 1e9:.2f} GB) through a 129 MB L2",
+                   "flags": flags},
+        "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_t64", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moe_w4a16.h -- C ABI of the routed-expert W4A16 MoE layer for GB300 (sm_103a).
+ *
+ * What the layer computes (sources are the pages describing the model):
+ *   - Shapes and weight format: "Kimi-K2.6" (model-catalog page), GEOMETRY,
+ *     QUANT and PARAMS paragraphs -- hidden 7168, 384 routed experts, 8 per
+ *     token, moe_intermediate_size 2048; the routed experts are an INT4 bank
+ *     (compressed-tensors, pack-quantized, symmetric, group size 32, int4
+ *     weights in int32 containers); one shared expert kept in higher precision.
+ *   - The routed MoE with its routing and W4A16 expert kernels:
+ *     "feat(pytorch): support Kimi K2.6", Motivation and Changes.
+ *   The pages do not spell out the router, the nibble order or the activation;
+ *   the readings this library implements are:
+ *     score_e = sigmoid(logit_e) in fp32 (a fixed sequence of IEEE fp32
+ *       operations, identical on every run and every device: see moe_route);
+ *     top-k by score, lowest expert index first on ties, weights renormalised
+ *       to sum to 1;
+ *     weight q in [-8, 7] stored as nibble q + 8, input 8c + j of a row in bits
+ *       4j..4j+3 of the row's int32 word c; one bf16 scale per 32 inputs;
+ *     expert(x) = W2 * (SiLU(W_gate x) .* (W_up x)),
+ *     out[t] = sum_j w[t,j] * expert_{id[t,j]}(x[t]) (+ shared(x[t])).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers unless the name ends in _host. bf16 values
+ *     travel as uint16_t bit patterns. Arrays are row-major, C-contiguous, the
+ *     input (K) dimension innermost. Device pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call is asynchronous and stream-ordered, unless documented otherwise.
+ *   - The caller owns every buffer. The library allocates no device memory,
+ *     keeps no per-call state, and holds only a per-device cache of device
+ *     properties and a process-wide launch counter.
+ *   - Argument and shape errors are returned synchronously, before anything
+ *     is launched. A failed launch returns MOE_ERR_CUDA. Errors found on the
+ *     device (an expert id out of range, a bounded wait that expired) are
+ *     recorded in the workspace status word and reported by moe_check_status.
+ *   - T == 0 is a no-op that returns MOE_OK.
+ *   - Shape rules: 1 <= top_k <= E <= 1024; H and I multiples of 32 in
+ *     [32, 32768]; group == 32; 0 <= T and T * top_k <= 2^24.
+ */
+#ifndef MOE_W4A16_H
+#define MOE_W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad op code    */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,    /* violates the shape rules above              */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < moe_workspace_size(...)          */
+  MOE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed           */
+  MOE_ERR_DEVICE_TIMEOUT = 5,       /* a bounded device wait expired (status word) */
+  MOE_ERR_DEVICE_BOUNDS = 6,        /* an expert id outside [0, E) (status word)   */
+  MOE_ERR_UNSUPPORTED_DEVICE = 7    /* not a compute capability 10.3 device        */
+} moe_status_t;
+
+/* Layer dimensions. group must be 32. */
+typedef struct {
+  int32_t E;      /* routed experts                    */
+  int32_t top_k;  /* experts per token                 */
+  int32_t H;      /* hidden size                       */
+  int32_t I;      /* expert intermediate size          */
+  int32_t group;  /* inputs per scale (32)             */
+} moe_dims_t;
+
+/* Weights of one layer (device pointers). Per expert e:
+ *   w13_packed[e] : int32 [2I][H/8]  rows 0..I-1 = gate, rows I..2I-1 = up
+ *   w13_scale[e]  : bf16  [2I][H/32]
+ *   w2_packed[e]  : int32 [H][I/8]
+ *   w2_scale[e]   : bf16  [H][I/32]
+ * Optional dense bf16 shared expert (both NULL and shared_I == 0 if absent):
+ *   shared_wgu    : bf16  [2*shared_I][H]  gate rows first
+ *   shared_wd     : bf16  [H][shared_I]
+ * shared_I must be a multiple of 64. */
+typedef struct {
+  const int32_t* w13_packed;
+  const uint16_t* w13_scale;
+  const int32_t* w2_packed;
+  const uint16_t* w2_scale;
+  const uint16_t* shared_wgu;
+  const uint16_t* shared_wd;
+  int32_t shared_I;
+} moe_weights_t;
+
+/* Grouped GEMM operations. */
+#define MOE_GEMM_GATEUP_SILU 0   /* h[r, :] = SiLU(W_gate a[r]) .* (W_up a[r]), out [R][I] */
+#define MOE_GEMM_DOWN 1          /* y[r, :] = W2 a[r],                          out [R][H] */
+
+/* Flags (bitwise OR). 0 selects the default tensor-core path. */
+#define MOE_FLAG_GEMM_SIMT 0x1u  /* grouped GEMMs on the CUDA-core baseline kernel        */
+#define MOE_FLAG_A_SMEM 0x2u     /* stage dequantised weights in shared memory, not TMEM  */
+/* Bits 8..15: token rows per tile of the tensor-core GEMM: 16, 32, 64 or 128
+ * (16 or 32 with MOE_FLAG_A_SMEM); 0 lets the library choose from T * top_k / E.
+ * Any other value makes the GEMM calls return MOE_ERR_UNSUPPORTED_SHAPE. */
+#define MOE_FLAG_TOKENS_PER_TILE(n) ((uint32_t)(n) << 8)
+
+/* Text of a status code (static storage; never NULL). */
+MOE_API const char* moe_status_string(moe_status_t s);
+
+/* Bytes of workspace that moe_forward / moe_forward_host need for T tokens
+ * (shared_I = 0 without a shared expert). A workspace of this size also serves
+ * every other entry point for the same dims and T. Returns 0 for invalid dims.
+ * Before its first use the first 256 bytes of a workspace must be zero. */
+MOE_API size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags);
+
+/* Step 1, routing. logits fp32 [T][E] -> topk_ids int32 [T][k] and topk_w fp32
+ * [T][k], in rank order (score descending, expert index ascending on ties).
+ * score = 1 / (1 + e(-logit)), every operation one IEEE fp32 operation rounded
+ * to nearest even, with e(t) = p(r) * 2^n, n = rint(t * log2 e),
+ * r = (t - n * LN2_HI) - n * LN2_LO (Cody-Waite split of ln 2, LN2_HI the
+ * multiple of 2^-14 nearest ln 2), p the degree-7 Taylor polynomial of exp in
+ * Horner form; e(t) = +inf for t > 88 and 0 for t < -87. NaN scores rank below
+ * all numbers. w_j = s_j / (s_0 + ... + s_{k-1}) (sum in rank order); all
+ * weights are 1/k when that sum is 0. Bit-identical on every device. */
+MOE_API moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
+                       int32_t* topk_ids, float* topk_w, void* stream);
+
+/* The router's score function alone, element-wise: scores[i] = score(logits[i]). */
+MOE_API moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream);
+
+/* Step 2, expert-sorted permutation. Assignment i = t*k + j goes to row
+ * inv_perm[i]; rows are grouped by expert, expert e owning rows
+ * [expert_offsets[e], expert_offsets[e+1]), and within an expert ordered by
+ * increasing i (a stable sort). sorted_token_ids[row] = the row's token.
+ *   topk_ids int32 [T][k] -> expert_offsets int32 [E+1], sorted_token_ids
+ *   int32 [T*k], inv_perm int32 [T*k].
+ * If x (bf16 [T][H]) and x_perm (bf16 [T*k][H]) are both non-NULL, also
+ * gathers x_perm[row] = x[sorted_token_ids[row]]. An id outside [0, E) sets
+ * MOE_ERR_DEVICE_BOUNDS in the status word and that assignment is left out
+ * (its inv_perm entry is -1; no out-of-bounds access). Deterministic: no
+ * result depends on timing. ws: status word in its first 256 bytes, then
+ * 4 * E * ceil(T*k / 4096) bytes of scratch (a moe_workspace_size workspace
+ * is large enough). */
+MOE_API moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
+                         int32_t* expert_offsets, int32_t* sorted_token_ids, int32_t* inv_perm,
+                         const uint16_t* x, int32_t H, uint16_t* x_perm,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 3 and 4, the grouped W4A16 GEMMs over expert-sorted rows. Row r of
+ * a_rows (bf16 [R][K], R = T*k) belongs to the expert e with
+ * expert_offsets[e] <= r < expert_offsets[e+1]. Each weight is dequantised as
+ * bf16(q * scale) and the products accumulate in fp32 on the tensor cores.
+ *   op = MOE_GEMM_GATEUP_SILU: K = H, out_rows bf16 [R][I],
+ *        out = bf16(SiLU(g) * u), g and u the gate and up rows of W13_e.
+ *   op = MOE_GEMM_DOWN:        K = I, out_rows bf16 [R][H], out = bf16(W2_e a).
+ * ws: the status word (its first 256 bytes). */
+MOE_API moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_t* w,
+                                    const uint16_t* a_rows, int32_t T,
+                                    const int32_t* expert_offsets, uint16_t* out_rows,
+                                    void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* The dense bf16 shared expert: out bf16 [T][H] = Wd (SiLU(Wg x) .* (Wu x)) for
+ * x bf16 [T][H], fp32 accumulation. Needs w->shared_wgu, w->shared_wd, and
+ * moe_workspace_size(d, T, w->shared_I, flags) bytes of workspace. */
+MOE_API moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T,
+                               uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Step 5, combine: out[t] = bf16( sum_j topk_w[t][j] * y[inv_perm[t*k+j]]
+ * (+ addend[t]) ), fp32 accumulation in rank order j, one rounding at the end.
+ * y_rows bf16 [T*k][H], addend bf16 [T][H] or NULL, out bf16 [T][H]. */
+MOE_API moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w,
+                         int32_t T, int32_t k, int32_t H, const uint16_t* addend,
+                         uint16_t* out, void* stream);
+
+/* The whole layer: route, permute (with gather), gate/up GEMM, down GEMM,
+ * the shared expert when w has one, combine.
+ *   x bf16 [T][H], logits fp32 [T][E] -> out bf16 [T][H].
+ * ws_bytes >= moe_workspace_size(d, T, w->shared_I, flags). */
+MOE_API moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits,
+                         int32_t T, uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags,
+                         void* stream);
+
+/* moe_forward from and to HOST buffers: copies x_host and logits_host into the
+ * workspace, runs the layer, copies the result to out_host, all enqueued on
+ * `stream`; the call returns before the copies finish (synchronise the stream
+ * before reading out_host). Host buffers should be page-locked for the copies
+ * to be asynchronous. ws_bytes >= moe_workspace_size(...) plus
+ * moe_host_staging_size(d, T). */
+MOE_API size_t moe_host_staging_size(moe_dims_t d, int32_t T);
+MOE_API moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host,
+                              const float* logits_host, int32_t T, uint16_t* out_host,
+                              void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Synchronises `stream`, reads the workspace status word, resets it to 0 and
+ * returns it (MOE_OK if no device error was recorded since the last check). */
+MOE_API moe_status_t moe_check_status(void* ws, void* stream);
+
+/* Number of kernels this library has launched in this process. */
+MOE_API uint64_t moe_launch_count(void);
+
+/* Self-test of the bounded device waits: launches one block that waits on a
+ * barrier nothing will complete, for at most timeout_ns (clamped to 1 ms ..
+ * 2 s), then records MOE_ERR_DEVICE_TIMEOUT in the status word and returns.
+ * The GPU stays usable. */
+MOE_API moe_status_t moe_debug_expire_wait(void* ws, int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4A16_H */

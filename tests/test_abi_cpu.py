@@ -1,0 +1,96 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "moe_w4a16.h")
+
+
+def declared_symbols():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_mixture_experts_sigmoid_gb300 import build as build_mod
+    build_mod.build()
+    from w4a16_mixture_experts_sigmoid_gb300 import binding
+    return binding.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    from w4a16_mixture_experts_sigmoid_gb300 import binding
+    assert sorted(binding.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    for code in range(8):
+        assert B.moe_status_string(code) and B.moe_status_string(code) != "unknown status"
+    assert B.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    d = B.dims(384, 8, 7168, 2048)
+    ws = B.moe_workspace_size(d, 64)
+    Tk = 64 * 8
+    # at least x_perm + h + y of the routed rows
+    assert ws >= Tk * 7168 * 2 * 2 + Tk * 2048 * 2
+    assert B.moe_workspace_size(d, 64, 2048) > ws
+    assert B.moe_workspace_size(B.dims(384, 8, 7168, 2040), 64) == 0        # I not a multiple of 32
+    assert B.moe_workspace_size(B.dims(2000, 8, 7168, 2048), 64) == 0       # E > 1024
+    assert B.moe_workspace_size(B.dims(8, 9, 256, 128), 4) == 0             # k > E
+    assert B.moe_workspace_size(B.dims(8, 2, 256, 128, 64), 4) == 0         # group != 32
+    assert B.moe_workspace_size(d, -1) == 0
+
+
+def test_arguments_rejected_before_any_launch(lib):
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    L = lib
+    assert L.moe_route(None, 4, 8, 2, None, None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route(16, -1, 8, 2, 16, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route(16, 4, 8, 9, 16, 16, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_route(16, 4, 2000, 2, 16, 16, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_route(16, 0, 8, 2, 16, 16, None) == B.MOE_OK                     # T == 0: no-op
+    assert L.moe_sigmoid_scores(None, 4, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, 16, 64, None, 16, 4096, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, None, 0, None, 16, 16, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    d = B.dims(8, 2, 256, 128)
+    w = B.moe_weights_t(16, 16, 16, 16, None, None, 0)
+    byref = ctypes.byref
+    assert L.moe_w4a16_grouped_gemm(7, d, byref(w), 16, 4, 16, 16, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_w4a16_grouped_gemm(0, B.dims(8, 2, 250, 128), byref(w), 16, 4, 16, 16, 16, 4096, 0, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_w4a16_grouped_gemm(0, d, None, 16, 4, 16, 16, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_w4a16_grouped_gemm(0, d, byref(w), 16, 4, 16, 16, 16, 8, 0, None) == \
+        B.MOE_ERR_WORKSPACE_TOO_SMALL
+    bad = B.moe_weights_t(16, 16, 16 + 4, 16, None, None, 0)                  # misaligned pointer
+    assert L.moe_w4a16_grouped_gemm(0, d, byref(bad), 16, 4, 16, 16, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG
+    half_shared = B.moe_weights_t(16, 16, 16, 16, 16, None, 64)
+    assert L.moe_forward(d, byref(half_shared), 16, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    odd_shared = B.moe_weights_t(16, 16, 16, 16, 16, 16, 96)
+    assert L.moe_forward(d, byref(odd_shared), 16, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_forward(d, byref(w), 16, 16, 4, 16, 16, 64, 0, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_forward(d, byref(w), 16, 16, 1 << 24, 16, 16, 1 << 40, 0, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_shared_expert(d, byref(w), 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(None, 16, 16, 4, 2, 256, None, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine(16, 16, 16, 4, 2, 250, None, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_check_status(None, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_expire_wait(None, 1000, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_host(d, byref(w), None, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_launch_count() == 0                                           # nothing launched

@@ -1,0 +1,74 @@
+// Step 5: the top-k weighted combine back to token order,
+//   out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]]  (+ addend[t]) ),
+// fp32 accumulation in rank order j, one rounding to bf16 at the end.
+// The pages' MoE sums the selected experts' outputs per token ("feat(pytorch):
+// support Kimi K2.6", MoE routing); where the weights enter is not spelled out,
+// and multiplying after the down projection is the reading used here.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// grid: (ceil(H/8 / blockDim), T); each thread owns 8 consecutive columns of one token.
+__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int T, int k, int H8,
+                                                      const uint4* __restrict__ addend, uint4* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= H8) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const int p = inv[(int64_t)t * k + j];
+    if (p < 0) continue;
+    const float wj = w[(int64_t)t * k + j];
+    float f[8];
+    unpack8(__ldg(y + (int64_t)p * H8 + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+  }
+  if (addend != nullptr) {
+    float f[8];
+    unpack8(__ldg(addend + (int64_t)t * H8 + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  out[(int64_t)t * H8 + c] = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
+                           const uint16_t* addend, uint16_t* out, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const int H8 = H / 8;
+  dim3 grid((H8 + 127) / 128, T < 65535 ? T : 65535);
+  combine_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const uint4*>(y), inv, w, T, k, H8,
+                                      reinterpret_cast<const uint4*>(addend), reinterpret_cast<uint4*>(out));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,623 @@
+// Steps 3 and 4 on the 5th-generation tensor cores: the grouped W4A16 expert
+// GEMMs over expert-sorted token rows, for sm_103a.
+//
+// Weight format ("Kimi-K2.6" catalog page, QUANT/PARAMS: int4 in int32
+// containers, symmetric, group 32): W[n, k] = q * s with q = nibble - 8,
+// nibble of input k = bits 4(k%8).. of word k/8 of row n, s the bf16 scale of
+// group k/32. Expert shapes (GEOMETRY): W13 = [gate; up] is [2I][H], W2 is [H][I].
+//
+// Orientation ("swap AB"): the MMA's M = 128 weight rows, its N = NT token
+// rows of one expert, K = the reduction dimension. A tile is one 128-row slab
+// of one expert's weights; a decode step touches ~1-3 tokens per expert, so
+// tokens are the narrow operand.
+//
+// One persistent CTA per SM, 12 warps:
+//   warp 0      TMA producer: int4 words + bf16 scales + token rows into a
+//               ring of STAGES shared-memory stages (128-byte swizzle).
+//   warp 1      MMA issuer (one thread): tcgen05.mma, fp32 accumulator in TMEM.
+//   warp 2      owns the tensor-memory allocation.
+//   warps 4-11  dequantise: each thread owns one weight row (= one TMEM lane)
+//               and half of a stage's K range; it turns 128 nibbles into
+//               bf16(q*s) and writes them to tensor memory (the MMA's A operand,
+//               default) or to shared memory in the swizzled K-major layout
+//               (MOE_FLAG_A_SMEM). Warps 4-7 also run the epilogue: TMEM ->
+//               registers -> SiLU(gate)*up (gate/up) or the plain row (down)
+//               -> bf16 rows in global memory.
+// Dense bf16 weights (the shared expert) skip the dequantiser: TMA loads the
+// weight tile straight into the swizzled layout.
+//
+// Gate/up pairing: within each 32-lane quarter q of the 128 lanes, lanes
+// 0-15 hold gate rows j0+16q+0..15 and lanes 16-31 the up rows with the same
+// j, so the epilogue pairs them with one shuffle.
+//
+// Every wait is bounded (mbar_wait): an expired wait records
+// MOE_ERR_DEVICE_TIMEOUT in the status word, every role leaves its loop, the
+// producer lets its copies in flight land, the MMA issuer lets its MMAs
+// finish, and the CTA frees its tensor memory before returning.
+#include "common.cuh"
+#include "internal.h"
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;            // weight rows per tile (MMA M)
+constexpr int BK = 256;            // K per pipeline stage
+constexpr int KSUB = 64;           // K per 128-byte swizzle row
+constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
+constexpr int kThreads = 384;
+constexpr int kFirstDqWarp = 4;
+constexpr int kDqWarps = 8;
+constexpr int kMaxE = 1024;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_100-class parts
+constexpr int kAlignSlack = 1024;
+constexpr int kAuxBytes = 7168;
+
+struct TcParams {
+  CUtensorMap tm_w;  // int4 words [rows_total][K/8] (box 32 x 64) or bf16 weights [rows_total][K] (box 64 x 16)
+  CUtensorMap tm_s;  // bf16 scales [rows_total][K/32] (box 8 x 64), when scale_tma
+  CUtensorMap tm_b;  // bf16 token rows [R][K] (box 64 x NT)
+  const uint16_t* scales;
+  const int32_t* offsets;
+  uint16_t* out;
+  int* status;
+  int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R;
+  unsigned long long timeout_ns;
+};
+
+template <int ASRC, int NT>
+struct Cfg {
+  static constexpr int kAStage = (ASRC == A_SMEM_BF16) ? NSUB * BM * 128 : BM * 128;
+  static constexpr int kBStage = NSUB * NT * 128;
+  static constexpr int kSStage = (ASRC == A_SMEM_BF16) ? 0 : BM * 16;
+  static constexpr int kStage = kAStage + kBStage + kSStage;
+  static constexpr int kNBuf = (ASRC == A_TMEM_DQ) ? (NT <= 128 ? 3 : 2) : (ASRC == A_SMEM_DQ ? 2 : 1);
+  static constexpr int kABuf = (ASRC == A_SMEM_DQ) ? NSUB * BM * 128 : 0;
+  static constexpr int kAvail = kSmemLimit - kAlignSlack - kAuxBytes - (ASRC == A_SMEM_DQ ? kNBuf * kABuf : 0);
+  static constexpr int kStagesRaw = kAvail / kStage;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
+  static constexpr int kColsNeeded = kAccCol + NT;
+  static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
+                                   : kColsNeeded <= 256 ? 256 : 512;
+  static constexpr int kSmemBytes = kAlignSlack + kStages * kStage + kNBuf * kABuf + kAuxBytes;
+  static_assert(kStages >= 2, "pipeline needs at least two stages");
+  static_assert(kColsNeeded <= 512, "tensor memory overflow");
+  static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+
+struct TileInfo {
+  int wt;      // weight tile (128 rows; for gate/up 64 gate + 64 up rows)
+  int e;       // expert
+  int row0;    // first token row of the chunk
+  int nvalid;  // token rows of the chunk that belong to the expert
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t* act_e, const int* tpre,
+                                                const TcParams& p, int nt) {
+  int lo = 0, hi = n_act - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tpre[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo t;
+  t.e = act_e[lo];
+  int start, cnt;
+  if (p.uniform_rows >= 0) { start = 0; cnt = p.uniform_rows; }
+  else { start = p.offsets[t.e]; cnt = p.offsets[t.e + 1] - start; }
+  const int nch = (cnt + nt - 1) / nt;
+  const int rem = i - tpre[lo];
+  t.wt = rem / nch;
+  const int c = rem - t.wt * nch;
+  t.row0 = start + c * nt;
+  t.nvalid = min(nt, cnt - c * nt);
+  return t;
+}
+
+// Bounded wait by every lane of a warp, with a warp-uniform verdict: lanes that
+// saw the phase complete and lanes that timed out or saw the abort flag agree
+// on one outcome, so no .sync.aligned instruction runs with part of the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const TcParams& p, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Four 32-bit words of int4 (one 32-input group, one scale) -> 16 bf16x2
+// registers holding bf16(q*s) for consecutive input pairs.
+__device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bits, uint32_t* out16) {
+  const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)),
+                                               __ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)));
+  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);  // 128 (magic exponent) + 8 (nibble bias)
+  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w = w4[i];
+    // bf16 0x43<nibble> = 128 + nibble exactly; each register gets nibbles m and m+4
+    const uint32_t p0 = (w & 0x000F000Fu) | 0x43004300u;
+    const uint32_t p1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+    const uint32_t pr[4] = {__byte_perm(p0, p1, 0x5410), __byte_perm(p2, p3, 0x5410), __byte_perm(p0, p1, 0x7632),
+                            __byte_perm(p2, p3, 0x7632)};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pr[m]);
+      v = __hmul2(__hsub2(v, off), s2);  // (128 + n - 136) exactly, then one rounding of q*s
+      out16[4 * i + m] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+  }
+}
+
+template <int OP, int ASRC, int NT>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<ASRC, NT>;
+  constexpr int S = C::kStages;
+  constexpr int NB = C::kNBuf;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* abuf = smem + S * C::kStage;
+  uint8_t* aux = abuf + NB * C::kABuf;
+  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* empty = full + S;
+  uint64_t* afull = empty + S;
+  uint64_t* aempty = afull + NB;
+  uint64_t* accfull = aempty + NB;
+  uint64_t* accempty = accfull + 1;
+  uint64_t* drain = accempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* n_act_s = reinterpret_cast<int*>(tmem_slot + 2);
+  int16_t* act_e = reinterpret_cast<int16_t*>(tmem_slot + 4);
+  int* tpre = reinterpret_cast<int*>(act_e + kMaxE);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_wt = (OP == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
+  const int nk = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 32); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < NB; ++b) { mbar_init(&afull[b], kDqWarps); mbar_init(&aempty[b], 1); }
+    mbar_init(accfull, 1);
+    mbar_init(accempty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == 3) {
+    // compact list of experts with rows, and the prefix of their tile counts
+    if (p.uniform_rows >= 0) {
+      if (lane == 0) {
+        const int chunks = (p.uniform_rows + NT - 1) / NT;
+        *n_act_s = p.uniform_rows > 0 ? 1 : 0;
+        act_e[0] = 0;
+        tpre[0] = 0;
+        tpre[1] = n_wt * chunks;
+        if (p.uniform_rows == 0) tpre[0] = 0;
+      }
+    } else {
+      int base_a = 0, base_t = 0;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        const int cnt = (e < p.E) ? p.offsets[e + 1] - p.offsets[e] : 0;
+        const bool f = cnt > 0;
+        const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) : 0;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
+        int incl = ntl;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += o;
+        }
+        if (f) {
+          const int pos = base_a + __popc(m & ((1u << lane) - 1u));
+          act_e[pos] = static_cast<int16_t>(e);
+          tpre[pos] = base_t + incl - ntl;
+        }
+        base_a += __popc(m);
+        base_t += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+      if (lane == 0) {
+        *n_act_s = base_a;
+        tpre[base_a] = base_t;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_act = *n_act_s;
+  const int total = tpre[n_act];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol_w = l2_policy_evict_first();
+    const uint64_t pol_b = l2_policy_evict_last();
+    constexpr uint32_t kTx = (ASRC == A_SMEM_BF16) ? (NSUB * BM * 128 + NSUB * NT * 128)
+                                                   : (BM * 128 + NSUB * NT * 128);
+    const uint32_t tx = kTx + ((ASRC != A_SMEM_BF16 && p.scale_tma) ? BM * 16 : 0);
+    const int kg = p.K / 32;
+    int g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+      const int ebase = ti.e * p.rows_per_expert;
+      int grow_lo, grow_hi;
+      if (OP == MOE_GEMM_GATEUP_SILU) { grow_lo = ebase + ti.wt * 64; grow_hi = ebase + p.out_cols + ti.wt * 64; }
+      else { grow_lo = ebase + ti.wt * BM; grow_hi = grow_lo + 64; }
+      for (int ks = 0; ks < nk; ++ks, ++g) {
+        const int s = g % S;
+        const uint32_t ph = (g / S) & 1;
+        if (!warp_wait(&empty[s], ph ^ 1, p, abort_flag)) { ok = false; break; }
+        uint8_t* sa = smem + s * C::kStage;
+        uint8_t* sb = sa + C::kAStage;
+        uint8_t* ss = sb + C::kBStage;
+        if (ASRC != A_SMEM_BF16 && !p.scale_tma) {
+          // scales by plain loads (row stride not 16-byte aligned): lane owns rows lane + 32 r
+          uint16_t* sc = reinterpret_cast<uint16_t*>(ss);
+          for (int r = lane; r < BM; r += 32) {
+            const int grow = (r < 64) ? grow_lo + r : grow_hi + (r - 64);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int gi = ks * 8 + q;
+              uint16_t v = 0;
+              if (gi < kg && grow < p.rows_total) v = p.scales[static_cast<int64_t>(grow) * kg + gi];
+              sc[r * 8 + q] = v;
+            }
+          }
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], tx);
+          if (ASRC == A_SMEM_BF16) {
+#pragma unroll
+            for (int sub = 0; sub < NSUB; ++sub) {
+#pragma unroll
+              for (int rb = 0; rb < 8; ++rb) {
+                int grow;
+                if (OP == MOE_GEMM_GATEUP_SILU) grow = (rb & 1) * p.out_cols + ti.wt * 64 + 16 * (rb >> 1);
+                else grow = ti.wt * BM + 16 * rb;
+                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, &full[s], ks * BK + sub * KSUB, grow, pol_w);
+              }
+            }
+          } else {
+            tma_load_2d(sa, &p.tm_w, &full[s], ks * (BK / 8), grow_lo, pol_w);
+            tma_load_2d(sa + 64 * 128, &p.tm_w, &full[s], ks * (BK / 8), grow_hi, pol_w);
+            if (p.scale_tma) {
+              tma_load_2d(ss, &p.tm_s, &full[s], ks * 8, grow_lo, pol_w);
+              tma_load_2d(ss + 64 * 16, &p.tm_s, &full[s], ks * 8, grow_hi, pol_w);
+            }
+          }
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, &full[s], ks * BK + sub * KSUB, ti.row0, pol_b);
+        } else {
+          mbar_arrive(&full[s]);
+        }
+      }
+    }
+    // let every copy issued into this CTA's shared memory land before exit
+    if (lane == 0) {
+      for (int d = 0; d < S && d < g; ++d) {
+        const int gg = g - 1 - d;
+        mbar_wait(&full[gg % S], (gg / S) & 1, p.timeout_ns, nullptr, p.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, NT);
+      const uint32_t d_tmem = tmem + C::kAccCol;
+      int g = 0, it = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
+        if (!mbar_wait(accempty, (it & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          const int s = g % S;
+          const uint32_t ph = (g / S) & 1;
+          const int b = g % NB;
+          const uint32_t pha = (g / NB) & 1;
+          if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          if (ASRC != A_SMEM_BF16) {
+            if (!mbar_wait(&afull[b], pha, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::kStage);
+          const uint32_t sb = sa + C::kAStage;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const int sub = kk >> 2;
+            const uint32_t koff = (kk & 3) * 32;
+            const uint64_t bdesc = sw128_kmajor_desc(sb + sub * (NT * 128) + koff);
+            const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+            if (ASRC == A_TMEM_DQ) {
+              mma_ts(d_tmem, tmem + b * 128 + kk * 8, bdesc, idesc, acc);
+            } else if (ASRC == A_SMEM_DQ) {
+              const uint64_t adesc = sw128_kmajor_desc(smem_u32(abuf + b * C::kABuf) + sub * (BM * 128) + koff);
+              mma_ss(d_tmem, adesc, bdesc, idesc, acc);
+            } else {
+              const uint64_t adesc = sw128_kmajor_desc(sa + sub * (BM * 128) + koff);
+              mma_ss(d_tmem, adesc, bdesc, idesc, acc);
+            }
+          }
+          mma_commit(&empty[s]);
+          if (ASRC != A_SMEM_BF16) mma_commit(&aempty[b]);
+        }
+        if (!ok) break;
+        mma_commit(accfull);
+      }
+      // let every MMA issued by this thread finish before tensor memory is freed
+      mma_commit(drain);
+      mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status);
+    }
+    __syncwarp();
+  } else if (warp >= kFirstDqWarp) {
+    // ------------------------------------------------------------ dequantise + epilogue
+    const int dw = warp - kFirstDqWarp;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int kh = dw >> 2;  // which half of the stage's K range
+    const int l = 32 * q + lane;
+    const int r_sm = (OP == MOE_GEMM_GATEUP_SILU) ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : l;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    int g = 0, it = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+      if (ASRC != A_SMEM_BF16) {
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          const int s = g % S;
+          const uint32_t ph = (g / S) & 1;
+          const int b = g % NB;
+          const uint32_t pha = (g / NB) & 1;
+          if (!warp_wait(&full[s], ph, p, abort_flag)) { ok = false; break; }
+          const uint8_t* arow = smem + s * C::kStage + r_sm * 128;
+          const uint8_t* srow = smem + s * C::kStage + C::kAStage + C::kBStage + r_sm * 16 + kh * 8;
+          uint4 wv[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = kh * 4 + cc;
+            wv[cc] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
+          }
+          const uint2 sv = *reinterpret_cast<const uint2*>(srow);
+          uint32_t dq[64];
+          dequant_group(wv[0], sv.x & 0xFFFFu, dq + 0);
+          dequant_group(wv[1], sv.x >> 16, dq + 16);
+          dequant_group(wv[2], sv.y & 0xFFFFu, dq + 32);
+          dequant_group(wv[3], sv.y >> 16, dq + 48);
+          if (!warp_wait(&aempty[b], pha ^ 1, p, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (ASRC == A_TMEM_DQ) {
+            const uint32_t ta = lane_base + b * 128 + kh * 64;
+            tmem_st16(ta + 0, dq + 0);
+            tmem_st16(ta + 16, dq + 16);
+            tmem_st16(ta + 32, dq + 32);
+            tmem_st16(ta + 48, dq + 48);
+            tmem_wait_st();
+          } else {
+            uint8_t* ab = abuf + b * C::kABuf;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+              const int sub = 2 * kh + (m >> 3);
+              const int ch = m & 7;
+              *reinterpret_cast<uint4*>(ab + sub * (BM * 128) + l * 128 + ((ch ^ (l & 7)) << 4)) =
+                  make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+            }
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afull[b]);
+        }
+        if (!ok) break;
+      }
+      if (kh == 0) {
+        // epilogue: accumulator lane l = weight row of this tile, columns = token rows
+        if (!warp_wait(accfull, it & 1, p, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int cb = 0; cb < NT; cb += 16) {
+          uint32_t v[16];
+          __syncwarp();
+          tmem_ld16(lane_base + C::kAccCol + cb, v);
+          tmem_wait_ld();
+          if (OP == MOE_GEMM_GATEUP_SILU) {
+            float u[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) u[c] = __shfl_down_sync(0xFFFFFFFFu, __uint_as_float(v[c]), 16);
+            const int j = ti.wt * 64 + 16 * q + lane;
+            if (lane < 16 && j < p.out_cols) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int row = ti.row0 + cb + c;
+                if (cb + c < ti.nvalid && row < p.R) {
+                  const float gt = __uint_as_float(v[c]);
+                  const float h = gt / (1.0f + __expf(-gt)) * u[c];
+                  p.out[static_cast<int64_t>(row) * p.out_cols + j] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
+                }
+              }
+            }
+          } else {
+            const int n = ti.wt * BM + l;
+            if (n < p.out_cols) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int row = ti.row0 + cb + c;
+                if (cb + c < ti.nvalid && row < p.R)
+                  p.out[static_cast<int64_t>(row) * p.out_cols + n] =
+                      __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(accempty);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                 uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int OP, int ASRC, int NT>
+cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
+  using C = Cfg<ASRC, NT>;
+  // the shared-memory opt-in is per device: remember it per device ordinal
+  static std::atomic<uint64_t> opted_in{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || !(opted_in.load() & bit)) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel<OP, ASRC, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    opted_in.fetch_or(bit);
+  }
+  tc_gemm_kernel<OP, ASRC, NT><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+template <int OP>
+cudaError_t dispatch(const TcParams& prm, int asrc, int nt, int grid, cudaStream_t s) {
+  switch (asrc) {
+    case A_TMEM_DQ:
+      switch (nt) {
+        case 16: return run<OP, A_TMEM_DQ, 16>(prm, grid, s);
+        case 32: return run<OP, A_TMEM_DQ, 32>(prm, grid, s);
+        case 64: return run<OP, A_TMEM_DQ, 64>(prm, grid, s);
+        case 128: return run<OP, A_TMEM_DQ, 128>(prm, grid, s);
+      }
+      break;
+    case A_SMEM_DQ:
+      switch (nt) {
+        case 16: return run<OP, A_SMEM_DQ, 16>(prm, grid, s);
+        case 32: return run<OP, A_SMEM_DQ, 32>(prm, grid, s);
+      }
+      break;
+    case A_SMEM_BF16:
+      switch (nt) {
+        case 16: return run<OP, A_SMEM_BF16, 16>(prm, grid, s);
+        case 32: return run<OP, A_SMEM_BF16, 32>(prm, grid, s);
+        case 64: return run<OP, A_SMEM_BF16, 64>(prm, grid, s);
+      }
+      break;
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, cudaStream_t s) {
+  if (p.R <= 0) return cudaSuccess;
+  if (p.bf16_weights != (asrc == A_SMEM_BF16)) return cudaErrorNotSupported;
+  if (!p.bf16_weights && p.E > kMaxE) return cudaErrorNotSupported;
+  TcParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int groups = p.uniform_rows >= 0 ? 1 : p.E;
+  const int64_t rows_total = static_cast<int64_t>(groups) * p.rows_per_expert;
+  bool ok;
+  if (p.bf16_weights) {
+    ok = make_map_2d(&prm.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w, p.K, rows_total, 2ull * p.K, KSUB, 16,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  } else {
+    ok = make_map_2d(&prm.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, p.w, p.K / 8, rows_total, p.K / 2, BK / 8, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+    prm.scale_tma = (p.K % 256 == 0) ? 1 : 0;
+    if (ok && prm.scale_tma)
+      ok = make_map_2d(&prm.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.scales, p.K / 32, rows_total, p.K / 16, 8, 64,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (ok)
+    ok = make_map_2d(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.R, 2ull * p.K, KSUB, nt,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
+  prm.scales = p.scales;
+  prm.offsets = p.offsets;
+  prm.out = p.out;
+  prm.status = p.status;
+  prm.E = p.E;
+  prm.K = p.K;
+  prm.rows_per_expert = p.rows_per_expert;
+  prm.out_cols = p.out_cols;
+  prm.uniform_rows = p.uniform_rows;
+  prm.rows_total = static_cast<int>(rows_total);
+  prm.R = p.R;
+  prm.timeout_ns = 2000000000ull;
+  // upper bound on tiles: every expert with rows contributes ceil(rows/nt) <= rows/nt + 1 chunks
+  const int n_wt = (p.op == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
+  const int64_t chunks = static_cast<int64_t>(p.R) / nt + (groups < p.R ? groups : p.R);
+  const int64_t tiles = chunks * n_wt;
+  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
+  if (p.op == MOE_GEMM_GATEUP_SILU) return dispatch<MOE_GEMM_GATEUP_SILU>(prm, asrc, nt, grid, s);
+  return dispatch<MOE_GEMM_DOWN>(prm, asrc, nt, grid, s);
+}
+
+// ---------------------------------------------------------------------------
+// self-test of the bounded waits: nothing ever arrives on this barrier
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void expire_wait_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, timeout_ns, &abort_flag, status);
+}
+}  // namespace
+
+cudaError_t launch_expire_wait(int* status, int64_t timeout_ns, cudaStream_t s) {
+  expire_wait_kernel<<<1, 32, 0, s>>>(status, static_cast<unsigned long long>(timeout_ns));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,56 @@
+// Host-side launchers of the kernels (one translation unit each), called by
+// the C-ABI layer in moe_abi.cu. Every launcher validates nothing: the ABI
+// layer checks arguments first. Each returns the launch's cudaError_t.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// counts kernels launched by this library (moe_launch_count)
+void count_launches(uint64_t n);
+
+// defined fp32 sigmoid + top-k routing
+cudaError_t launch_sigmoid(const float* logits, int64_t n, float* scores, cudaStream_t s);
+cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+
+// expert-sorted permutation (count, scan, scatter) and row gather
+int permute_blocks(int64_t Tk);  // number of segments of the count/scatter kernels
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets, int32_t* sorted_ids,
+                           int32_t* inv_perm, int32_t* hist, int* status, cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const int32_t* offsets, int E, int R,
+                          int H, uint16_t* x_perm, cudaStream_t s);
+
+// combine
+cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
+                           const uint16_t* addend, uint16_t* out, cudaStream_t s);
+
+// grouped GEMM problem description shared by both GEMM implementations
+struct GemmProblem {
+  int op;                  // MOE_GEMM_GATEUP_SILU or MOE_GEMM_DOWN
+  bool bf16_weights;       // dense bf16 weights (shared expert) instead of int4
+  const void* w;           // int32 [E][rows][K/8] or bf16 [rows][K]
+  const uint16_t* scales;  // bf16 [E][rows][K/32] (int4 only)
+  const uint16_t* a;       // bf16 [R][K], expert-sorted rows
+  const int32_t* offsets;  // [E+1], or null with uniform_rows >= 0
+  uint16_t* out;           // bf16 [R][out_cols]
+  int* status;
+  int E;
+  int K;
+  int rows_per_expert;     // 2I (gate/up) or H (down)
+  int out_cols;            // I (gate/up) or H (down)
+  int R;                   // rows of a and out
+  int uniform_rows;        // >= 0: a single group of that many rows
+};
+
+cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t s);
+
+enum ASource { A_TMEM_DQ = 0, A_SMEM_DQ = 1, A_SMEM_BF16 = 2 };
+// returns cudaErrorNotSupported if no kernel exists for (asrc, tokens_per_tile)
+cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int tokens_per_tile, int num_sms, cudaStream_t s);
+
+cudaError_t launch_expire_wait(int* status, int64_t timeout_ns, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,420 @@
+// The C ABI of the library (declared in include/moe_w4a16.h): argument and
+// shape validation before any launch, the workspace layout, the per-device
+// property cache, and the launch sequence of moe_forward. Everything that
+// computes runs in the kernels of the other translation units.
+#include "common.cuh"
+#include "internal.h"
+
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+}  // namespace moe
+
+namespace {
+
+using namespace moe;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxRows = int64_t(1) << 24;  // T * top_k
+constexpr int kMaxDim = 32768;                  // H, I, shared_I
+
+struct DevInfo {
+  int sms = 0;
+  bool supported = false;
+};
+
+DevInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+moe_status_t current_device(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::call_once(g_dev_once[dev], [dev] {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_dev[dev].sms = sms;
+    g_dev[dev].supported = (major == 10 && minor == 3);
+  });
+  *out = g_dev[dev];
+  return out->supported ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+moe_status_t check_dims(const moe_dims_t& d) {
+  if (d.E < 1 || d.E > 1024 || d.top_k < 1 || d.top_k > d.E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.group != 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.H < 32 || d.H % 32 || d.H > kMaxDim || d.I < 32 || d.I % 32 || d.I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status_t check_T(int32_t T, int32_t k) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * k > kMaxRows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status_t check_weights(const moe_weights_t* w, bool need_shared) {
+  if (w == nullptr || w->w13_packed == nullptr || w->w13_scale == nullptr || w->w2_packed == nullptr ||
+      w->w2_scale == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w13_packed) || !aligned16(w->w13_scale) || !aligned16(w->w2_packed) || !aligned16(w->w2_scale))
+    return MOE_ERR_INVALID_ARG;
+  const bool has_shared = w->shared_wgu != nullptr || w->shared_wd != nullptr || w->shared_I != 0;
+  if (has_shared || need_shared) {
+    if (w->shared_wgu == nullptr || w->shared_wd == nullptr || !aligned16(w->shared_wgu) || !aligned16(w->shared_wd))
+      return MOE_ERR_INVALID_ARG;
+    if (w->shared_I < 64 || w->shared_I % 64 || w->shared_I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  return MOE_OK;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Workspace layout of moe_forward (byte offsets, each 256-aligned).
+struct Layout {
+  size_t ids, w, offsets, sorted, inv, hist, xperm, h, y, hs, ys, end;
+};
+
+Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
+  Layout L;
+  const size_t Tk = static_cast<size_t>(T) * d.top_k;
+  size_t off = 256;  // status word
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.ids = take(Tk * 4);
+  L.w = take(Tk * 4);
+  L.offsets = take(static_cast<size_t>(d.E + 1) * 4);
+  L.sorted = take(Tk * 4);
+  L.inv = take(Tk * 4);
+  L.hist = take(static_cast<size_t>(permute_blocks(static_cast<int64_t>(Tk))) * d.E * 4);
+  L.xperm = take(Tk * d.H * 2);
+  L.h = take(Tk * d.I * 2);
+  L.y = take(Tk * d.H * 2);
+  L.hs = take(static_cast<size_t>(T) * shared_I * 2);
+  L.ys = take(shared_I > 0 ? static_cast<size_t>(T) * d.H * 2 : 0);
+  L.end = off;
+  return L;
+}
+
+int auto_tokens_per_tile(int64_t rows, int groups) {
+  const double m = static_cast<double>(rows) / (groups > 0 ? groups : 1);
+  if (m <= 8.0) return 16;
+  if (m <= 18.0) return 32;
+  if (m <= 40.0) return 64;
+  return 128;
+}
+
+moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights_t* w, const uint16_t* a,
+                              int32_t T, const int32_t* offsets, uint16_t* out, int* status, uint32_t flags,
+                              int sms, cudaStream_t s) {
+  GemmProblem p;
+  p.op = op;
+  p.bf16_weights = false;
+  p.a = a;
+  p.offsets = offsets;
+  p.out = out;
+  p.status = status;
+  p.E = d.E;
+  p.R = T * d.top_k;
+  p.uniform_rows = -1;
+  if (op == MOE_GEMM_GATEUP_SILU) {
+    p.w = w->w13_packed;
+    p.scales = w->w13_scale;
+    p.K = d.H;
+    p.rows_per_expert = 2 * d.I;
+    p.out_cols = d.I;
+  } else {
+    p.w = w->w2_packed;
+    p.scales = w->w2_scale;
+    p.K = d.I;
+    p.rows_per_expert = d.H;
+    p.out_cols = d.H;
+  }
+  if (flags & MOE_FLAG_GEMM_SIMT) return cuda_status(launch_gemm_simt(p, s));
+  const int asrc = (flags & MOE_FLAG_A_SMEM) ? A_SMEM_DQ : A_TMEM_DQ;
+  int nt = static_cast<int>((flags >> 8) & 0xFFu);
+  if (nt == 0) {
+    nt = auto_tokens_per_tile(p.R, d.E);
+    if (asrc == A_SMEM_DQ && nt > 32) nt = 32;
+  }
+  const cudaError_t e = launch_gemm_tc(p, asrc, nt, sms, s);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(e);
+}
+
+moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* hs,
+                        uint16_t* out, int* status, uint32_t flags, int sms, cudaStream_t s) {
+  const int Is = w->shared_I;
+  GemmProblem p;
+  p.bf16_weights = true;
+  p.scales = nullptr;
+  p.offsets = nullptr;
+  p.status = status;
+  p.E = 1;
+  p.R = T;
+  p.uniform_rows = T;
+  // gate/up: [T][H] -> hs [T][Is]
+  p.op = MOE_GEMM_GATEUP_SILU;
+  p.w = w->shared_wgu;
+  p.a = x;
+  p.out = hs;
+  p.K = d.H;
+  p.rows_per_expert = 2 * Is;
+  p.out_cols = Is;
+  const int nt = T <= 16 ? 16 : (T <= 32 ? 32 : 64);
+  cudaError_t e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
+  // down: hs [T][Is] -> out [T][H]
+  p.op = MOE_GEMM_DOWN;
+  p.w = w->shared_wd;
+  p.a = hs;
+  p.out = out;
+  p.K = Is;
+  p.rows_per_expert = d.H;
+  p.out_cols = d.H;
+  e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, const float* logits,
+                            int32_t T, uint16_t* out, uint8_t* ws, uint32_t flags, int sms, cudaStream_t s) {
+  const Layout L = layout(d, T, w->shared_I);
+  int* status = reinterpret_cast<int*>(ws);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
+  float* tw = reinterpret_cast<float*>(ws + L.w);
+  int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+  int32_t* sorted = reinterpret_cast<int32_t*>(ws + L.sorted);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+  int32_t* hist = reinterpret_cast<int32_t*>(ws + L.hist);
+  uint16_t* xperm = reinterpret_cast<uint16_t*>(ws + L.xperm);
+  uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
+  uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
+  const int R = T * d.top_k;
+  cudaError_t e = launch_route(logits, T, d.E, d.top_k, ids, tw, s);
+  if (e == cudaSuccess) e = launch_permute(ids, T, d.E, d.top_k, offsets, sorted, inv, hist, status, s);
+  if (e == cudaSuccess) e = launch_gather(x, sorted, offsets, d.E, R, d.H, xperm, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, sms, s);
+  if (st != MOE_OK) return st;
+  st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags, sms, s);
+  if (st != MOE_OK) return st;
+  const uint16_t* addend = nullptr;
+  if (w->shared_wgu != nullptr) {
+    uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
+    uint16_t* ys = reinterpret_cast<uint16_t*>(ws + L.ys);
+    st = run_shared(d, w, x, T, hs, ys, status, flags, sms, s);
+    if (st != MOE_OK) return st;
+    addend = ys;
+  }
+  return cuda_status(launch_combine(y, inv, tw, T, d.top_k, d.H, addend, out, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "expert id out of range";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags) {
+  (void)flags;
+  if (check_dims(d) != MOE_OK || check_T(T, d.top_k) != MOE_OK || shared_I < 0) return 0;
+  return layout(d, T, shared_I).end;
+}
+
+size_t moe_host_staging_size(moe_dims_t d, int32_t T) {
+  if (check_dims(d) != MOE_OK || check_T(T, d.top_k) != MOE_OK) return 0;
+  return align256(static_cast<size_t>(T) * d.H * 2) * 2 + align256(static_cast<size_t>(T) * d.E * 4);
+}
+
+moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids, float* topk_w,
+                       void* stream) {
+  if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_route(logits, T, E, k, topk_ids, topk_w, as_stream(stream)));
+}
+
+moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream) {
+  if (logits == nullptr || scores == nullptr || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_sigmoid(logits, n, scores, as_stream(stream)));
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t* expert_offsets,
+                         int32_t* sorted_token_ids, int32_t* inv_perm, const uint16_t* x, int32_t H,
+                         uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (topk_ids == nullptr || expert_offsets == nullptr || sorted_token_ids == nullptr || inv_perm == nullptr ||
+      ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const bool gather = x != nullptr && x_perm != nullptr;
+  if ((x != nullptr) != (x_perm != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (gather && (H < 8 || H % 8 || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const int64_t Tk = static_cast<int64_t>(T) * k;
+  const size_t need = 256 + static_cast<size_t>(permute_blocks(Tk)) * E * 4;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = launch_permute(topk_ids, T, E, k, expert_offsets, sorted_token_ids, inv_perm,
+                                 reinterpret_cast<int32_t*>(w8 + 256), reinterpret_cast<int*>(w8), s);
+  if (e == cudaSuccess && gather)
+    e = launch_gather(x, sorted_token_ids, expert_offsets, E, static_cast<int>(Tk), H, x_perm, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_t* w, const uint16_t* a_rows,
+                                    int32_t T, const int32_t* expert_offsets, uint16_t* out_rows, void* ws,
+                                    size_t ws_bytes, uint32_t flags, void* stream) {
+  if (op != MOE_GEMM_GATEUP_SILU && op != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (a_rows == nullptr || expert_offsets == nullptr || out_rows == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a_rows) || !aligned16(out_rows)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, out_rows, static_cast<int*>(ws), flags, di.sms,
+                          as_stream(stream));
+}
+
+moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* out,
+                               void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if (w == nullptr) return MOE_ERR_INVALID_ARG;
+  if (w->shared_wgu == nullptr || w->shared_wd == nullptr || !aligned16(w->shared_wgu) || !aligned16(w->shared_wd))
+    return MOE_ERR_INVALID_ARG;
+  if (w->shared_I < 64 || w->shared_I % 64 || w->shared_I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (x == nullptr || out == nullptr || ws == nullptr || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(d, T, w->shared_I);
+  if (ws_bytes < L.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return run_shared(d, w, x, T, reinterpret_cast<uint16_t*>(w8 + L.hs), out, reinterpret_cast<int*>(w8), flags,
+                    di.sms, as_stream(stream));
+}
+
+moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w, int32_t T, int32_t k,
+                         int32_t H, const uint16_t* addend, uint16_t* out, void* stream) {
+  if (y_rows == nullptr || inv_perm == nullptr || topk_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || k < 1 || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_rows) || !aligned16(out) || (addend != nullptr && !aligned16(addend))) return MOE_ERR_INVALID_ARG;
+  if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, out, as_stream(stream)));
+}
+
+moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits, int32_t T,
+                         uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (x == nullptr || logits == nullptr || out == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout(d, T, w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  return forward_device(d, w, x, logits, T, out, static_cast<uint8_t*>(ws), flags, di.sms, as_stream(stream));
+}
+
+moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host, const float* logits_host,
+                              int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes, uint32_t flags,
+                              void* stream) {
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (x_host == nullptr || logits_host == nullptr || out_host == nullptr || ws == nullptr || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const size_t base = layout(d, T, w->shared_I).end;
+  if (ws_bytes < base + moe_host_staging_size(d, T)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (T == 0) return MOE_OK;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  const size_t xb = static_cast<size_t>(T) * d.H * 2, lb = static_cast<size_t>(T) * d.E * 4;
+  uint16_t* dx = reinterpret_cast<uint16_t*>(w8 + base);
+  float* dl = reinterpret_cast<float*>(w8 + base + align256(xb));
+  uint16_t* dout = reinterpret_cast<uint16_t*>(w8 + base + align256(xb) + align256(lb));
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(dl, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  st = forward_device(d, w, dx, dl, T, dout, w8, flags, di.sms, s);
+  if (st != MOE_OK) return st;
+  return cuda_status(cudaMemcpyAsync(out_host, dout, xb, cudaMemcpyDeviceToHost, s));
+}
+
+moe_status_t moe_check_status(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(v);
+}
+
+uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_debug_expire_wait(void* ws, int64_t timeout_ns, void* stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (timeout_ns < 1000000) timeout_ns = 1000000;
+  if (timeout_ns > 2000000000) timeout_ns = 2000000000;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_expire_wait(static_cast<int*>(ws), timeout_ns, as_stream(stream)));
+}
+
+}  // extern "C"

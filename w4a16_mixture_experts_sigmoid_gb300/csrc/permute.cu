@@ -1,0 +1,168 @@
+// Step 2: the expert-sorted permutation of the T*k (token, expert) assignments
+// and the gather of activation rows into that order.
+//
+// Assignment i = t*k + j. Row order = stable sort of the assignments by
+// expert id: every result is a pure function of topk_ids, independent of
+// scheduling (the only atomics are order-free counts).
+//
+//   count   (one block per segment of kSeg assignments): per-segment histogram.
+//   scan    (one block): per-expert prefix over segments, then offsets[E+1].
+//   scatter (one block per segment): per-warp histograms and bases, then each
+//           warp walks its slice 32 assignments at a time in order, ranking
+//           equal ids with __match_any_sync.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kSeg = 4096;        // assignments per segment
+constexpr int kScatterWarps = 8;  // warps per scatter block, each owns kSeg / 8 assignments
+
+__global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ ids, int64_t Tk, int E,
+                                                    int32_t* __restrict__ hist, int* status) {
+  extern __shared__ int32_t h[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+  __syncthreads();
+  const int64_t lo = (int64_t)blockIdx.x * kSeg;
+  const int64_t hi = min(Tk, lo + kSeg);
+  bool bad = false;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
+    else bad = true;
+  }
+  if (bad) record_status(status, MOE_ERR_DEVICE_BOUNDS);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = h[e];
+}
+
+// hist[b][e] <- number of assignments to e in segments < b (exclusive over b);
+// offsets <- exclusive scan of per-expert totals.
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E,
+                                                    int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_sum[32];
+  const int e = threadIdx.x;
+  int32_t run = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int32_t c = hist[(int64_t)b * E + e];
+      hist[(int64_t)b * E + e] = run;
+      run += c;
+    }
+  }
+  // block-wide exclusive scan of run over e (E <= 1024 = blockDim)
+  const int lane = e & 31, warp = e >> 5;
+  int32_t v = (e < E) ? run : 0;
+  int32_t incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t ws = warp_sum[lane];
+    int32_t wi = ws;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int32_t o = __shfl_up_sync(0xFFFFFFFFu, wi, off);
+      if (lane >= off) wi += o;
+    }
+    warp_sum[lane] = wi - ws;  // exclusive prefix of warps
+  }
+  __syncthreads();
+  const int32_t excl = warp_sum[warp] + incl - v;
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + v;
+}
+
+__global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32_t* __restrict__ ids, int64_t Tk,
+                                                                     int k, int E,
+                                                                     const int32_t* __restrict__ hist,
+                                                                     const int32_t* __restrict__ offsets,
+                                                                     int32_t* __restrict__ sorted_ids,
+                                                                     int32_t* __restrict__ inv) {
+  extern __shared__ int32_t wb[];  // [kScatterWarps][E]: per-warp counts, then per-warp bases
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wb[i] = 0;
+  __syncthreads();
+  constexpr int kSlice = kSeg / kScatterWarps;
+  const int64_t lo = (int64_t)blockIdx.x * kSeg + (int64_t)warp * kSlice;
+  const int64_t hi = min(Tk, lo + kSlice);
+  for (int64_t i = lo + lane; i < hi; i += 32) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&wb[warp * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t base = offsets[e] + hist[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int32_t c = wb[w * E + e];
+      wb[w * E + e] = base;
+      base += c;
+    }
+  }
+  __syncthreads();
+  int32_t* mybase = wb + warp * E;
+  for (int64_t i0 = lo; i0 < hi; i0 += 32) {
+    const int64_t i = i0 + lane;
+    int e = (i < hi) ? ids[i] : -1;
+    const bool ok = (e >= 0 && e < E);
+    if (!ok) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int32_t pos = 0;
+    if (ok) pos = mybase[e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) mybase[e] += __popc(peers);
+    __syncwarp();
+    if (ok) {
+      sorted_ids[pos] = static_cast<int32_t>(i / k);
+      inv[i] = pos;
+    } else if (i < hi) {
+      inv[i] = -1;
+    }
+  }
+}
+
+// x_perm[row] = x[sorted_ids[row]] for rows < offsets[E]; 16-byte copies.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
+                                                     const int32_t* __restrict__ offsets, int E, int R, int H8,
+                                                     uint4* __restrict__ xp) {
+  const int valid = offsets[E];
+  for (int row = blockIdx.x; row < R && row < valid; row += gridDim.x) {
+    const uint4* src = x + (int64_t)sorted_ids[row] * H8;
+    uint4* dst = xp + (int64_t)row * H8;
+    for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = __ldg(src + c);
+  }
+}
+
+}  // namespace
+
+int permute_blocks(int64_t Tk) { return static_cast<int>((Tk + kSeg - 1) / kSeg); }
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets, int32_t* sorted_ids,
+                           int32_t* inv_perm, int32_t* hist, int* status, cudaStream_t s) {
+  const int64_t Tk = (int64_t)T * k;
+  const int nblk = permute_blocks(Tk);
+  count_kernel<<<nblk, 256, sizeof(int32_t) * E, s>>>(ids, Tk, E, hist, status);
+  scan_kernel<<<1, 1024, 0, s>>>(hist, nblk, E, offsets);
+  scatter_kernel<<<nblk, kScatterWarps * 32, sizeof(int32_t) * kScatterWarps * E, s>>>(ids, Tk, k, E, hist, offsets,
+                                                                                     sorted_ids, inv_perm);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const int32_t* offsets, int E, int R, int H,
+                          uint16_t* x_perm, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const int blocks = R < 4096 ? R : 4096;
+  gather_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
+                                       reinterpret_cast<uint4*>(x_perm));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,77 @@
+"""One routed-expert W4A16 MoE layer resident on the GPU.
+
+Holds the layer's device weights and a workspace; every call goes through
+the C ABI (moe_forward / moe_forward_host). PyTorch only provides device
+memory and the stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoeW4A16Layer:
+    def __init__(self, E: int, top_k: int, H: int, I: int, w13, s13, w2, s2, shared_wgu=None, shared_wd=None,
+                 device="cuda"):
+        def dev(a, dtype):
+            if a is None:
+                return None
+            t = torch.as_tensor(a) if not isinstance(a, torch.Tensor) else a
+            return t.to(device=device, dtype=dtype).contiguous()
+
+        self.E, self.top_k, self.H, self.I = E, top_k, H, I
+        self.w13 = dev(w13, torch.int32)
+        self.s13 = dev(s13, torch.int16)   # bf16 bit patterns
+        self.w2 = dev(w2, torch.int32)
+        self.s2 = dev(s2, torch.int16)
+        self.sh_gu = dev(shared_wgu, torch.int16)
+        self.sh_d = dev(shared_wd, torch.int16)
+        self.dims = B.dims(E, top_k, H, I)
+        self.weights = B.weights(self.w13, self.s13, self.w2, self.s2, self.sh_gu, self.sh_d)
+        self.shared_I = 0 if self.sh_d is None else int(self.sh_d.shape[1])
+        self._ws = None
+        self._ws_T = -1
+        self.device = device
+
+    @classmethod
+    def from_arrays(cls, shape, arrays: dict, device="cuda"):
+        import numpy as np
+
+        def t(key):
+            a = arrays.get(key)
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            return torch.from_numpy(a)
+
+        return cls(shape.E, shape.top_k, shape.H, shape.I, t("w13"), t("s13"), t("w2"), t("s2"), t("sh_gu"),
+                   t("sh_d"), device=device)
+
+    def workspace(self, T: int, host_staging: bool = False) -> torch.Tensor:
+        need = B.moe_workspace_size(self.dims, T, self.shared_I)
+        if host_staging:
+            need += B.moe_host_staging_size(self.dims, T)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None, flags: int = 0,
+                stream=None) -> torch.Tensor:
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.int16, device=self.device)
+        ws = self.workspace(T)
+        B.moe_forward(self.dims, self.weights, x, logits, T, out, ws, flags, stream)
+        return out
+
+    def forward_host(self, x_host, logits_host, out_host, flags: int = 0, stream=None):
+        T = int(x_host.shape[0])
+        ws = self.workspace(T, host_staging=True)
+        B.moe_forward_host(self.dims, self.weights, x_host, logits_host, T, out_host, ws, flags, stream)
+        return out_host
+
+    def check_status(self, stream=None) -> int:
+        return 0 if self._ws is None else B.moe_check_status(self._ws, stream)
