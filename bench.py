@@ -40,6 +40,9 @@ WORKLOADS = {
     "decode_t64": dict(shape=synth.FULL, T=64, skew=None),
     "prefill_t4096_zipf": dict(shape=synth.FULL, T=4096, skew=1.1),
     "tiny": dict(shape=synth.TINY, T=16, skew=None),
+    # profiling-sized decode: 48 full-size experts (1.2 GB of int4 + scales, ~9x L2), T=8 -> 1.33 rows per
+    # expert as in decode_t64; used for ncu captures that must stay a few GB on the device
+    "decode_e48_t8": dict(shape=synth.LayerShape(E=48, top_k=8, H=7168, I=2048), T=8, skew=None),
     "decode_t1_shared": dict(shape=synth.FULL_WITH_SHARED, T=1, skew=None),
     "decode_t8_shared": dict(shape=synth.FULL_WITH_SHARED, T=8, skew=None),
     "decode_t32_shared": dict(shape=synth.FULL_WITH_SHARED, T=32, skew=None),

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close_rms, bf16_dev_to_f32, dev
+from tests.gpu_util import assert_close_rows, bf16_dev_to_f32, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -71,8 +71,8 @@ def test_grouped_gemms_match_oracle(cuda_lib, shape, impl):
     B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, d, w, dev(a_gu), T, off, h, ws, flags)
     B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(a_dn), T, off, y, ws, flags)
     assert B.moe_check_status(ws) == B.MOE_OK
-    assert_close_rms(bf16_dev_to_f32(h), ref_h, what=f"gate/up {impl}")
-    assert_close_rms(bf16_dev_to_f32(y), ref_y, what=f"down {impl}")
+    assert_close_rows(bf16_dev_to_f32(h), ref_h, what=f"gate/up {impl}")
+    assert_close_rows(bf16_dev_to_f32(y), ref_y, what=f"down {impl}")
 
 
 def test_unsupported_tile_size_is_rejected(cuda_lib):

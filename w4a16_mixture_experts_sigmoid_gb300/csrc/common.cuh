@@ -9,7 +9,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/moe_w4a16.h"
+#include "moe_w4a16.h"
 
 namespace moe {
 

@@ -255,10 +255,10 @@ size_t moe_host_staging_size(moe_dims_t d, int32_t T) {
 
 moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids, float* topk_w,
                        void* stream) {
-  if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
+  if (logits == nullptr || topk_ids == nullptr || topk_w == nullptr) return MOE_ERR_INVALID_ARG;
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
@@ -266,8 +266,9 @@ moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int
 }
 
 moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream) {
-  if (logits == nullptr || scores == nullptr || n < 0) return MOE_ERR_INVALID_ARG;
+  if (n < 0) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
+  if (logits == nullptr || scores == nullptr) return MOE_ERR_INVALID_ARG;
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
@@ -277,16 +278,16 @@ moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, v
 moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t* expert_offsets,
                          int32_t* sorted_token_ids, int32_t* inv_perm, const uint16_t* x, int32_t H,
                          uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream) {
-  if (topk_ids == nullptr || expert_offsets == nullptr || sorted_token_ids == nullptr || inv_perm == nullptr ||
-      ws == nullptr)
-    return MOE_ERR_INVALID_ARG;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (topk_ids == nullptr || expert_offsets == nullptr || sorted_token_ids == nullptr || inv_perm == nullptr ||
+      ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
   const bool gather = x != nullptr && x_perm != nullptr;
   if ((x != nullptr) != (x_perm != nullptr)) return MOE_ERR_INVALID_ARG;
   if (gather && (H < 8 || H % 8 || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
   const int64_t Tk = static_cast<int64_t>(T) * k;
   const size_t need = 256 + static_cast<size_t>(permute_blocks(Tk)) * E * 4;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -310,11 +311,11 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
   if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
   if (a_rows == nullptr || expert_offsets == nullptr || out_rows == nullptr || ws == nullptr)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(a_rows) || !aligned16(out_rows)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < 256) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (T == 0) return MOE_OK;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, out_rows, static_cast<int*>(ws), flags, di.sms,
@@ -330,10 +331,10 @@ moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint1
   if (w->shared_wgu == nullptr || w->shared_wd == nullptr || !aligned16(w->shared_wgu) || !aligned16(w->shared_wd))
     return MOE_ERR_INVALID_ARG;
   if (w->shared_I < 64 || w->shared_I % 64 || w->shared_I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
   if (x == nullptr || out == nullptr || ws == nullptr || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   const Layout L = layout(d, T, w->shared_I);
   if (ws_bytes < L.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (T == 0) return MOE_OK;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -343,11 +344,11 @@ moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint1
 
 moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w, int32_t T, int32_t k,
                          int32_t H, const uint16_t* addend, uint16_t* out, void* stream) {
-  if (y_rows == nullptr || inv_perm == nullptr || topk_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
   if (T < 0 || k < 1 || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(y_rows) || !aligned16(out) || (addend != nullptr && !aligned16(addend))) return MOE_ERR_INVALID_ARG;
   if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
+  if (y_rows == nullptr || inv_perm == nullptr || topk_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_rows) || !aligned16(out) || (addend != nullptr && !aligned16(addend))) return MOE_ERR_INVALID_ARG;
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
@@ -360,10 +361,10 @@ moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
   if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
   if (x == nullptr || logits == nullptr || out == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < layout(d, T, w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (T == 0) return MOE_OK;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   return forward_device(d, w, x, logits, T, out, static_cast<uint8_t*>(ws), flags, di.sms, as_stream(stream));
@@ -376,11 +377,11 @@ moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
   if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
   if (x_host == nullptr || logits_host == nullptr || out_host == nullptr || ws == nullptr || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
   const size_t base = layout(d, T, w->shared_I).end;
   if (ws_bytes < base + moe_host_staging_size(d, T)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (T == 0) return MOE_OK;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
