@@ -306,8 +306,10 @@ def run_ours(args):
     h = torch.empty((R, s.I), dtype=torch.int16, device=dev)
     y = torch.empty((R, s.H), dtype=torch.int16, device=dev)
     wsp = layer.workspace(T)
+    # the split calls chain as moe_forward runs them: rows in the tensor-core K order unless on the CUDA-core path
+    order = 0 if (flags & B.MOE_FLAG_GEMM_SIMT) else B.MOE_FLAG_ROWS_MMA_ORDER
     B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
-    B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp)
+    B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp, order)
     torch.cuda.synchronize(dev)
     counts = np.diff(d_off.cpu().numpy())
     touched = int((counts > 0).sum())
@@ -354,11 +356,12 @@ def run_ours(args):
         E_[0].record(stream)
         B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
         E_[1].record(stream)
-        B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp)
+        B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp, order)
         E_[2].record(stream)
-        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp, flags)
+        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp,
+                                 flags | order)
         E_[3].record(stream)
-        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags)
+        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags | order)
         E_[4].record(stream)
         B.moe_combine(y, d_inv, d_w, T, s.top_k, s.H, None, out)
         E_[5].record(stream)

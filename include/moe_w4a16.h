@@ -99,6 +99,13 @@ typedef struct {
 /* Flags (bitwise OR). 0 selects the default tensor-core path. */
 #define MOE_FLAG_GEMM_SIMT 0x1u  /* grouped GEMMs on the CUDA-core baseline kernel        */
 #define MOE_FLAG_A_SMEM 0x2u     /* stage dequantised weights in shared memory, not TMEM  */
+/* Activation rows exchanged between the steps are stored in the tensor-core
+ * GEMM's K order: inside every block of 8 consecutive inputs, position p holds
+ * input [0,4,1,5,2,6,3,7][p]. With this flag moe_permute writes x_perm that way
+ * and moe_w4a16_grouped_gemm reads a_rows that way and (gate/up) writes h that
+ * way, so the calls chain exactly as moe_forward runs them; without it every
+ * row is in natural order. */
+#define MOE_FLAG_ROWS_MMA_ORDER 0x4u
 /* Bits 8..15: token rows per tile of the tensor-core GEMM: 16, 32, 64 or 128
  * (16 or 32 with MOE_FLAG_A_SMEM); 0 lets the library choose from T * top_k / E.
  * Any other value makes the GEMM calls return MOE_ERR_UNSUPPORTED_SHAPE. */
@@ -140,11 +147,12 @@ MOE_API moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* s
  * (its inv_perm entry is -1; no out-of-bounds access). Deterministic: no
  * result depends on timing. ws: status word in its first 256 bytes, then
  * 4 * E * ceil(T*k / 4096) bytes of scratch (a moe_workspace_size workspace
- * is large enough). */
+ * is large enough). flags: MOE_FLAG_ROWS_MMA_ORDER stores x_perm rows in the
+ * tensor-core K order. */
 MOE_API moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
                          int32_t* expert_offsets, int32_t* sorted_token_ids, int32_t* inv_perm,
                          const uint16_t* x, int32_t H, uint16_t* x_perm,
-                         void* ws, size_t ws_bytes, void* stream);
+                         void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /* Steps 3 and 4, the grouped W4A16 GEMMs over expert-sorted rows. Row r of
  * a_rows (bf16 [R][K], R = T*k) belongs to the expert e with
@@ -153,7 +161,12 @@ MOE_API moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, 
  *   op = MOE_GEMM_GATEUP_SILU: K = H, out_rows bf16 [R][I],
  *        out = bf16(SiLU(g) * u), g and u the gate and up rows of W13_e.
  *   op = MOE_GEMM_DOWN:        K = I, out_rows bf16 [R][H], out = bf16(W2_e a).
- * ws: the status word (its first 256 bytes). */
+ * flags: MOE_FLAG_GEMM_SIMT, MOE_FLAG_A_SMEM, MOE_FLAG_TOKENS_PER_TILE(n),
+ * MOE_FLAG_ROWS_MMA_ORDER (a_rows and, for gate/up, out_rows in the tensor-core
+ * K order). ws: the status word in its first 256 bytes; the tensor-core path
+ * with natural-order rows also rewrites a_rows into the K order right after
+ * it, so ws_bytes >= 256 + R*K*2 (rounded up to 256) unless
+ * MOE_FLAG_ROWS_MMA_ORDER or MOE_FLAG_GEMM_SIMT is set. */
 MOE_API moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_t* w,
                                     const uint16_t* a_rows, int32_t T,
                                     const int32_t* expert_offsets, uint16_t* out_rows,

@@ -46,20 +46,17 @@ def assert_close_rms(got, ref, max_rel=MAX_REL, mean_rel=MEAN_REL, what=""):
     assert err.mean() <= mean_rel * r, f"{what}: mean|err|/rms = {err.mean() / r:.3e}"
 
 
-# Intermediate rows of the grouped GEMMs (h = SiLU(g) * u, y = W2 h) are stored
-# in bf16 and are heavy-tailed (h is a product of two near-Gaussian values:
-# max|h| is ~20 RMS), so their own storage rounding (half a bf16 ulp, 2^-9
-# relative) can exceed a fixed fraction of the RMS. Their bound is per
-# element: twice that rounding of the value itself, plus 1e-2 RMS for the
-# bf16(q * s) weight rounding accumulated over K (~2^-9 / sqrt(3) RMS).
-def assert_close_rows(got, ref, rel=2.0 ** -8, abs_rms=1e-2, mean_rel=MEAN_REL, what=""):
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    assert got.shape == ref.shape, (got.shape, ref.shape)
-    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    r = rms(ref)
-    err = np.abs(got - ref)
-    bound = rel * np.abs(ref) + abs_rms * r
-    worst = np.unravel_index(np.argmax(err - bound), err.shape)
-    assert np.all(err <= bound), f"{what}: err {err[worst]:.3e} > bound {bound[worst]:.3e} at {worst}"
-    assert err.mean() <= mean_rel * r, f"{what}: mean|err|/rms = {err.mean() / r:.3e}"
+# The gate/up intermediate h = SiLU(g) * u is a product of two near-Gaussian
+# dot products (max |h| ~ 15-20 RMS). Its error is driven by the bf16(q * s)
+# weight rounding of g and u (relative 2^-9 per weight, ~2^-9/sqrt(3) of a
+# K-term dot product's size), multiplied by the other factor, so it scales with
+# |g| and |u| rather than with |h|. Emulating exactly that arithmetic on the CPU
+# (bf16 weights, exact accumulation, bf16 output) gives max |err| up to
+# 0.053 RMS(h) on the test shapes, mean 0.0015 RMS; the bound for h is
+# 8e-2 RMS max (1.5x that), 5e-3 RMS mean. The down rows y = W2 h are near
+# Gaussian and keep the layer's own bound (emulated max 0.017 RMS).
+H_MAX_REL = 8e-2
+
+
+def assert_close_h(got, ref, what=""):
+    assert_close_rms(got, ref, max_rel=H_MAX_REL, mean_rel=MEAN_REL, what=what)

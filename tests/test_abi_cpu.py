@@ -68,8 +68,8 @@ def test_arguments_rejected_before_any_launch(lib):
     assert L.moe_route(16, 4, 2000, 2, 16, 16, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_route(16, 0, 8, 2, 16, 16, None) == B.MOE_OK                     # T == 0: no-op
     assert L.moe_sigmoid_scores(None, 4, 16, None) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, 16, 64, None, 16, 4096, None) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, None, 0, None, 16, 16, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, 16, 64, None, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_permute(16, 4, 8, 2, 16, 16, 16, None, 0, None, 16, 16, 0, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
     d = B.dims(8, 2, 256, 128)
     w = B.moe_weights_t(16, 16, 16, 16, None, None, 0)
     byref = ctypes.byref
@@ -78,6 +78,9 @@ def test_arguments_rejected_before_any_launch(lib):
         B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_w4a16_grouped_gemm(0, d, None, 16, 4, 16, 16, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_w4a16_grouped_gemm(0, d, byref(w), 16, 4, 16, 16, 16, 8, 0, None) == \
+        B.MOE_ERR_WORKSPACE_TOO_SMALL
+    # natural-order rows on the tensor-core path need room to rewrite them: 256 + R*K*2 bytes
+    assert L.moe_w4a16_grouped_gemm(0, d, byref(w), 16, 4, 16, 16, 16, 256 + 8 * 256 * 2 - 16, 0, None) == \
         B.MOE_ERR_WORKSPACE_TOO_SMALL
     bad = B.moe_weights_t(16, 16, 16 + 4, 16, None, None, 0)                  # misaligned pointer
     assert L.moe_w4a16_grouped_gemm(0, d, byref(bad), 16, 4, 16, 16, 16, 4096, 0, None) == B.MOE_ERR_INVALID_ARG

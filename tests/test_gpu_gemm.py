@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close_rows, bf16_dev_to_f32, dev
+from tests.gpu_util import assert_close_h, assert_close_rms, bf16_dev_to_f32, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -64,15 +64,15 @@ def test_grouped_gemms_match_oracle(cuda_lib, shape, impl):
     d = B.dims(E, k, H, I)
     tens = {key: dev(v) for key, v in layer.items()}
     w = B.weights(tens["w13"], tens["s13"], tens["w2"], tens["s2"])
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(B.moe_workspace_size(d, T), dtype=torch.uint8, device="cuda")
     off = dev(offsets)
     h = torch.full((R, I), 0x7FC0, dtype=torch.int16, device="cuda")     # NaN fill: unwritten rows show up
     y = torch.full((R, H), 0x7FC0, dtype=torch.int16, device="cuda")
     B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, d, w, dev(a_gu), T, off, h, ws, flags)
     B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(a_dn), T, off, y, ws, flags)
     assert B.moe_check_status(ws) == B.MOE_OK
-    assert_close_rows(bf16_dev_to_f32(h), ref_h, what=f"gate/up {impl}")
-    assert_close_rows(bf16_dev_to_f32(y), ref_y, what=f"down {impl}")
+    assert_close_h(bf16_dev_to_f32(h), ref_h, what=f"gate/up {impl}")
+    assert_close_rms(bf16_dev_to_f32(y), ref_y, what=f"down {impl}")
 
 
 def test_unsupported_tile_size_is_rejected(cuda_lib):
@@ -81,9 +81,72 @@ def test_unsupported_tile_size_is_rejected(cuda_lib):
     layer, offsets, a_gu, _, _, _ = problem(*SHAPES[0])
     tens = {key: dev(v) for key, v in layer.items()}
     w = B.weights(tens["w13"], tens["s13"], tens["w2"], tens["s2"])
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     h = torch.empty((32, 128), dtype=torch.int16, device="cuda")
     for flags in (B.MOE_FLAG_TOKENS_PER_TILE(48), B.MOE_FLAG_A_SMEM | B.MOE_FLAG_TOKENS_PER_TILE(64)):
         with pytest.raises(B.MoeError) as e:
             B.moe_w4a16_grouped_gemm(0, B.dims(8, 2, 256, 128), w, dev(a_gu), 16, dev(offsets), h, ws, flags)
         assert e.value.code == B.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("simt", [False, True])
+def test_split_calls_in_mma_order_chain_like_forward(cuda_lib, simt):
+    """route -> permute -> gate/up -> down -> combine with the tensor-core K order
+    for the exchanged rows gives exactly the bits of moe_forward."""
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer
+    E, k, H, I, T = 33, 5, 288, 96, 37
+    shape = synth.LayerShape(E=E, top_k=k, H=H, I=I)
+    arrays = synth.make_layer(shape, seed=3)
+    x, logits = synth.make_tokens(T, H, E, seed=4)
+    layer = MoeW4A16Layer.from_arrays(shape, arrays)
+    flags = B.MOE_FLAG_GEMM_SIMT if simt else 0
+    ref = layer.forward(dev(x), dev(logits), flags=flags).clone()
+    R = T * k
+    ws = torch.zeros(B.moe_workspace_size(layer.dims, T), dtype=torch.uint8, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    srt = torch.empty(R, dtype=torch.int32, device="cuda")
+    inv = torch.empty(R, dtype=torch.int32, device="cuda")
+    xp = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    h = torch.empty((R, I), dtype=torch.int16, device="cuda")
+    y = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    order = 0 if simt else B.MOE_FLAG_ROWS_MMA_ORDER
+    B.moe_route(dev(logits), T, E, k, ids, w)
+    B.moe_permute(ids, T, E, k, off, srt, inv, dev(x), H, xp, ws, order)
+    B.moe_w4a16_grouped_gemm(0, layer.dims, layer.weights, xp, T, off, h, ws, flags | order)
+    B.moe_w4a16_grouped_gemm(1, layer.dims, layer.weights, h, T, off, y, ws, flags | order)
+    B.moe_combine(y, inv, w, T, k, H, None, out)
+    assert B.moe_check_status(ws) == B.MOE_OK
+    assert torch.equal(out, ref)
+
+
+def test_mma_order_rows_give_the_same_products(cuda_lib):
+    """The same rows handed over in natural order (converted inside) and in the
+    tensor-core K order give bit-identical GEMM outputs."""
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    E, k, H, I, T, skew = SHAPES[1]
+    layer, offsets, a_gu, a_dn, _, _ = problem(*SHAPES[1])
+    tens = {key: dev(v) for key, v in layer.items()}
+    w = B.weights(tens["w13"], tens["s13"], tens["w2"], tens["s2"])
+    d = B.dims(E, k, H, I)
+    R = T * k
+    ws = torch.zeros(B.moe_workspace_size(d, T), dtype=torch.uint8, device="cuda")
+    perm = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+    def mma(a):
+        K = a.shape[1]
+        return a.reshape(R, K // 8, 8)[:, :, perm].reshape(R, K)
+    y0 = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    y1 = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    B.moe_w4a16_grouped_gemm(1, d, w, dev(a_dn), T, dev(offsets), y0, ws, 0)
+    B.moe_w4a16_grouped_gemm(1, d, w, dev(mma(a_dn)), T, dev(offsets), y1, ws, B.MOE_FLAG_ROWS_MMA_ORDER)
+    assert torch.equal(y0, y1)
+    h0 = torch.empty((R, I), dtype=torch.int16, device="cuda")
+    h1 = torch.empty((R, I), dtype=torch.int16, device="cuda")
+    B.moe_w4a16_grouped_gemm(0, d, w, dev(a_gu), T, dev(offsets), h0, ws, 0)
+    B.moe_w4a16_grouped_gemm(0, d, w, dev(mma(a_gu)), T, dev(offsets), h1, ws, B.MOE_FLAG_ROWS_MMA_ORDER)
+    assert torch.equal(dev(mma(h0.cpu().numpy())), h1)     # h comes back in the same K order

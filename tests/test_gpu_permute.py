@@ -24,7 +24,14 @@ def run_permute(B, ids: np.ndarray, E: int, H: int = 64, gather: bool = True):
         xp = torch.zeros((T * k, H), dtype=torch.int16, device="cuda")
     B.moe_permute(idd, T, E, k, off, srt, inv, x, H, xp, ws)
     status = B.moe_check_status(ws)
-    return host(off), host(srt), host(inv), (host(xp, np.uint16) if gather else None), xh, status
+    xp_nat = host(xp, np.uint16).copy() if gather else None
+    if gather:
+        # the same gather in the tensor-core K order: every block of 8 inputs as [0,4,1,5,2,6,3,7]
+        B.moe_permute(idd, T, E, k, off, srt, inv, x, H, xp, ws, B.MOE_FLAG_ROWS_MMA_ORDER)
+        got = host(xp, np.uint16)
+        perm = np.array([0, 4, 1, 5, 2, 6, 3, 7])
+        assert np.array_equal(got, xp_nat.reshape(T * k, H // 8, 8)[:, :, perm].reshape(T * k, H))
+    return host(off), host(srt), host(inv), xp_nat, xh, status
 
 
 @pytest.mark.parametrize("T,E,k,skew", [(16, 8, 2, None), (64, 384, 8, None), (4096, 384, 8, None),

@@ -28,6 +28,7 @@ MOE_GEMM_DOWN = 1
 
 MOE_FLAG_GEMM_SIMT = 0x1
 MOE_FLAG_A_SMEM = 0x2
+MOE_FLAG_ROWS_MMA_ORDER = 0x4
 
 
 def MOE_FLAG_TOKENS_PER_TILE(n: int) -> int:
@@ -51,7 +52,7 @@ SIGNATURES = {
     "moe_route": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "moe_sigmoid_scores": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
-                              c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_void_p]),
+                              c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_w4a16_grouped_gemm": (c_int32, [c_int32, moe_dims_t, POINTER(moe_weights_t), c_void_p, c_int32,
                                          c_void_p, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_shared_expert": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_int32, c_void_p,
@@ -166,9 +167,9 @@ def moe_sigmoid_scores(logits, n: int, scores, stream=None) -> None:
 
 
 def moe_permute(topk_ids, T: int, E: int, k: int, expert_offsets, sorted_token_ids, inv_perm, x, H: int,
-                x_perm, ws, stream=None) -> None:
+                x_perm, ws, flags: int = 0, stream=None) -> None:
     _check(load().moe_permute(_dptr(topk_ids), T, E, k, _dptr(expert_offsets), _dptr(sorted_token_ids),
-                              _dptr(inv_perm), _dptr(x), H, _dptr(x_perm), _dptr(ws), _nbytes(ws),
+                              _dptr(inv_perm), _dptr(x), H, _dptr(x_perm), _dptr(ws), _nbytes(ws), flags,
                               _stream(stream)), "moe_permute")
 
 

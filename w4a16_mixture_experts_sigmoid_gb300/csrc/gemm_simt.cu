@@ -65,11 +65,14 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_simt_kernel(GemmProblem p) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float x0 = __uint_as_float(u[i] << 16), x1 = __uint_as_float(u[i] & 0xFFFF0000u);
-            acc_a[t] = fmaf(wa[2 * i], x0, acc_a[t]);
-            acc_a[t] = fmaf(wa[2 * i + 1], x1, acc_a[t]);
+            // the pair holds inputs (2i, 2i+1) in natural order, (i, i+4) in MMA K order
+            const int k0 = p.a_mma_order ? i : 2 * i;
+            const int k1 = p.a_mma_order ? i + 4 : 2 * i + 1;
+            acc_a[t] = fmaf(wa[k0], x0, acc_a[t]);
+            acc_a[t] = fmaf(wa[k1], x1, acc_a[t]);
             if (OP == MOE_GEMM_GATEUP_SILU) {
-              acc_b[t] = fmaf(wb[2 * i], x0, acc_b[t]);
-              acc_b[t] = fmaf(wb[2 * i + 1], x1, acc_b[t]);
+              acc_b[t] = fmaf(wb[k0], x0, acc_b[t]);
+              acc_b[t] = fmaf(wb[k1], x1, acc_b[t]);
             }
           }
         }
@@ -92,7 +95,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_simt_kernel(GemmProblem p) {
         } else {
           v = acc_a[t];
         }
-        p.out[static_cast<int64_t>(t0 + t) * p.out_cols + unit] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        int col = unit;
+        if (OP == MOE_GEMM_GATEUP_SILU && p.out_mma_order) col = (unit & ~7) | ((unit & 3) << 1) | ((unit >> 2) & 1);
+        p.out[static_cast<int64_t>(t0 + t) * p.out_cols + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
       }
     }
   }

@@ -9,22 +9,34 @@
 // Orientation ("swap AB"): the MMA's M = 128 weight rows, its N = NT token
 // rows of one expert, K = the reduction dimension. A tile is one 128-row slab
 // of one expert's weights; a decode step touches ~1-3 tokens per expert, so
-// tokens are the narrow operand.
+// tokens are the narrow operand. On this part an M=128, K=16 MMA costs the
+// same ~45 cycles for every N <= 64 (it is bound by reading the 128x16 A tile),
+// so the MMA count, not N, sets the tensor-core floor of a decode step.
 //
-// One persistent CTA per SM, 12 warps:
+// K order inside the MMA: each int32 word's eight nibbles are turned into four
+// bf16 pairs with one AND/OR each, pair m holding inputs m and m+4 of the
+// word. The MMA therefore sees the K order [0,4,1,5,2,6,3,7] inside every
+// block of 8 inputs. A dot product does not depend on the order of its terms,
+// so the token rows (operand B) are stored in the same order ("MMA order"):
+// the gather writes x rows that way and the gate/up epilogue writes h that
+// way, at no extra cost.
+//
+// One persistent CTA per SM, 16 warps:
 //   warp 0      TMA producer: int4 words + bf16 scales + token rows into a
 //               ring of STAGES shared-memory stages (128-byte swizzle).
-//   warp 1      MMA issuer (one thread): tcgen05.mma, fp32 accumulator in TMEM.
-//   warp 2      owns the tensor-memory allocation.
-//   warps 4-11  dequantise: each thread owns one weight row (= one TMEM lane)
-//               and half of a stage's K range; it turns 128 nibbles into
-//               bf16(q*s) and writes them to tensor memory (the MMA's A operand,
-//               default) or to shared memory in the swizzled K-major layout
-//               (MOE_FLAG_A_SMEM). Warps 4-7 also run the epilogue: TMEM ->
-//               registers -> SiLU(gate)*up (gate/up) or the plain row (down)
-//               -> bf16 rows in global memory.
+//   warp 1      MMA issuer (one thread): tcgen05.mma, fp32 accumulators in TMEM.
+//   warp 2      owns the tensor-memory allocation; warp 3 builds the tile list.
+//   warps 4-11  dequantise, in two groups of four that take alternate stages:
+//               each thread owns one weight row (= one TMEM lane) of its
+//               group's stage and turns its 256 nibbles into bf16(q*s) in the
+//               MMA's A operand: tensor memory (default) or swizzled shared
+//               memory (MOE_FLAG_A_SMEM).
+//   warps 12-15 epilogue: TMEM -> registers -> SiLU(gate)*up (gate/up) or the
+//               plain row (down) -> bf16 rows in global memory. Accumulators
+//               are double-buffered, so the epilogue of one tile overlaps the
+//               MMAs of the next.
 // Dense bf16 weights (the shared expert) skip the dequantiser: TMA loads the
-// weight tile straight into the swizzled layout.
+// weight tile straight into the swizzled layout (natural K order).
 //
 // Gate/up pairing: within each 32-lane quarter q of the 128 lanes, lanes
 // 0-15 hold gate rows j0+16q+0..15 and lanes 16-31 the up rows with the same
@@ -48,9 +60,9 @@ constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BK = 256;            // K per pipeline stage
 constexpr int KSUB = 64;           // K per 128-byte swizzle row
 constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kFirstDqWarp = 4;
-constexpr int kDqWarps = 8;
+constexpr int kFirstEpiWarp = 12;
 constexpr int kMaxE = 1024;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_100-class parts
 constexpr int kAlignSlack = 1024;
@@ -64,7 +76,7 @@ struct TcParams {
   const int32_t* offsets;
   uint16_t* out;
   int* status;
-  int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R;
+  int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
   unsigned long long timeout_ns;
 };
 
@@ -74,13 +86,13 @@ struct Cfg {
   static constexpr int kBStage = NSUB * NT * 128;
   static constexpr int kSStage = (ASRC == A_SMEM_BF16) ? 0 : BM * 16;
   static constexpr int kStage = kAStage + kBStage + kSStage;
-  static constexpr int kNBuf = (ASRC == A_TMEM_DQ) ? (NT <= 128 ? 3 : 2) : (ASRC == A_SMEM_DQ ? 2 : 1);
+  static constexpr int kNBuf = (ASRC == A_TMEM_DQ) ? (NT <= 64 ? 3 : 2) : (ASRC == A_SMEM_DQ ? 2 : 1);
   static constexpr int kABuf = (ASRC == A_SMEM_DQ) ? NSUB * BM * 128 : 0;
   static constexpr int kAvail = kSmemLimit - kAlignSlack - kAuxBytes - (ASRC == A_SMEM_DQ ? kNBuf * kABuf : 0);
   static constexpr int kStagesRaw = kAvail / kStage;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
-  static constexpr int kColsNeeded = kAccCol + NT;
+  static constexpr int kColsNeeded = kAccCol + 2 * NT;   // two accumulators
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
                                    : kColsNeeded <= 256 ? 256 : 512;
   static constexpr int kSmemBytes = kAlignSlack + kStages * kStage + kNBuf * kABuf + kAuxBytes;
@@ -126,8 +138,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-// Four 32-bit words of int4 (one 32-input group, one scale) -> 16 bf16x2
-// registers holding bf16(q*s) for consecutive input pairs.
+// One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
+// 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
+// 8i+m (low half) and 8i+m+4 (high half) of the chunk.
 __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bits, uint32_t* out16) {
   const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)),
                                                __ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)));
@@ -136,21 +149,19 @@ __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bi
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t w = w4[i];
-    // bf16 0x43<nibble> = 128 + nibble exactly; each register gets nibbles m and m+4
-    const uint32_t p0 = (w & 0x000F000Fu) | 0x43004300u;
-    const uint32_t p1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-    const uint32_t p2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-    const uint32_t p3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
-    const uint32_t pr[4] = {__byte_perm(p0, p1, 0x5410), __byte_perm(p2, p3, 0x5410), __byte_perm(p0, p1, 0x7632),
-                            __byte_perm(p2, p3, 0x7632)};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pr[m]);
-      v = __hmul2(__hsub2(v, off), s2);  // (128 + n - 136) exactly, then one rounding of q*s
+      // bf16 bit pattern 0x43<nibble> is exactly 128 + nibble
+      const uint32_t pr = ((w >> (4 * m)) & 0x000F000Fu) | 0x43004300u;
+      __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pr);
+      v = __hmul2(__hsub2(v, off), s2);  // (128 + n - 136) = q exactly, then one rounding of q*s
       out16[4 * i + m] = *reinterpret_cast<const uint32_t*>(&v);
     }
   }
 }
+
+// position of input j inside its block of 8 when a row is stored in MMA order
+__device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1); }
 
 template <int OP, int ASRC, int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
@@ -165,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint64_t* empty = full + S;
   uint64_t* afull = empty + S;
   uint64_t* aempty = afull + NB;
-  uint64_t* accfull = aempty + NB;
-  uint64_t* accempty = accfull + 1;
-  uint64_t* drain = accempty + 1;
+  uint64_t* accfull = aempty + NB;   // [2]
+  uint64_t* accempty = accfull + 2;  // [2]
+  uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* n_act_s = reinterpret_cast<int*>(tmem_slot + 2);
@@ -180,9 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) { mbar_init(&full[s], 32); mbar_init(&empty[s], 1); }
-    for (int b = 0; b < NB; ++b) { mbar_init(&afull[b], kDqWarps); mbar_init(&aempty[b], 1); }
-    mbar_init(accfull, 1);
-    mbar_init(accempty, 4);
+    for (int b = 0; b < NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], 4); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -197,7 +207,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         act_e[0] = 0;
         tpre[0] = 0;
         tpre[1] = n_wt * chunks;
-        if (p.uniform_rows == 0) tpre[0] = 0;
       }
     } else {
       int base_a = 0, base_t = 0;
@@ -312,12 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, NT);
-      const uint32_t d_tmem = tmem + C::kAccCol;
       int g = 0, it = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
-        if (!mbar_wait(accempty, (it & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
+        const int ab = it & 1;
+        if (!mbar_wait(&accempty[ab], ((it >> 1) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
         tc_fence_after();
+        const uint32_t d_tmem = tmem + C::kAccCol + ab * NT;
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = g % S;
           const uint32_t ph = (g / S) & 1;
@@ -350,115 +360,120 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (ASRC != A_SMEM_BF16) mma_commit(&aempty[b]);
         }
         if (!ok) break;
-        mma_commit(accfull);
+        mma_commit(&accfull[ab]);
       }
       // let every MMA issued by this thread finish before tensor memory is freed
       mma_commit(drain);
       mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status);
     }
     __syncwarp();
-  } else if (warp >= kFirstDqWarp) {
-    // ------------------------------------------------------------ dequantise + epilogue
-    const int dw = warp - kFirstDqWarp;
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int kh = dw >> 2;  // which half of the stage's K range
-    const int l = 32 * q + lane;
-    const int r_sm = (OP == MOE_GEMM_GATEUP_SILU) ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : l;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    int g = 0, it = 0;
-    bool ok = true;
-    for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
-      if (ASRC != A_SMEM_BF16) {
+  } else if (warp >= kFirstDqWarp && warp < kFirstEpiWarp) {
+    // ------------------------------------------------------------ dequantise
+    if (ASRC != A_SMEM_BF16) {
+      const int grp = (warp - kFirstDqWarp) >> 2;  // takes the stages g with g % 2 == grp
+      const int q = warp & 3;                      // TMEM lane quarter this warp may access
+      const int l = 32 * q + lane;
+      const int r_sm = (OP == MOE_GEMM_GATEUP_SILU) ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : l;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      int g = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
         for (int ks = 0; ks < nk; ++ks, ++g) {
+          if ((g & 1) != grp) continue;
           const int s = g % S;
           const uint32_t ph = (g / S) & 1;
           const int b = g % NB;
           const uint32_t pha = (g / NB) & 1;
           if (!warp_wait(&full[s], ph, p, abort_flag)) { ok = false; break; }
           const uint8_t* arow = smem + s * C::kStage + r_sm * 128;
-          const uint8_t* srow = smem + s * C::kStage + C::kAStage + C::kBStage + r_sm * 16 + kh * 8;
+          const uint4 sv = *reinterpret_cast<const uint4*>(smem + s * C::kStage + C::kAStage + C::kBStage + r_sm * 16);
+          const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
           uint4 wv[4];
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int c = kh * 4 + cc;
-            wv[cc] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
-          }
-          const uint2 sv = *reinterpret_cast<const uint2*>(srow);
-          uint32_t dq[64];
-          dequant_group(wv[0], sv.x & 0xFFFFu, dq + 0);
-          dequant_group(wv[1], sv.x >> 16, dq + 16);
-          dequant_group(wv[2], sv.y & 0xFFFFu, dq + 32);
-          dequant_group(wv[3], sv.y >> 16, dq + 48);
+          for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
           if (!warp_wait(&aempty[b], pha ^ 1, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
-          if (ASRC == A_TMEM_DQ) {
-            const uint32_t ta = lane_base + b * 128 + kh * 64;
-            tmem_st16(ta + 0, dq + 0);
-            tmem_st16(ta + 16, dq + 16);
-            tmem_st16(ta + 32, dq + 32);
-            tmem_st16(ta + 48, dq + 48);
-            tmem_wait_st();
-          } else {
-            uint8_t* ab = abuf + b * C::kABuf;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-              const int sub = 2 * kh + (m >> 3);
-              const int ch = m & 7;
-              *reinterpret_cast<uint4*>(ab + sub * (BM * 128) + l * 128 + ((ch ^ (l & 7)) << 4)) =
-                  make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+          for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                wv[c] = *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
             }
-            fence_proxy_async_smem();
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c = half * 4 + cc;
+              uint32_t dq[16];
+              dequant_group(wv[cc], (c & 1) ? (sw[c >> 1] >> 16) : (sw[c >> 1] & 0xFFFFu), dq);
+              if (ASRC == A_TMEM_DQ) {
+                tmem_st16(lane_base + b * 128 + c * 16, dq);
+              } else {
+                uint8_t* ab = abuf + b * C::kABuf + (c >> 1) * (BM * 128) + l * 128;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                  *reinterpret_cast<uint4*>(ab + ((((c & 1) * 4 + m) ^ (l & 7)) << 4)) =
+                      make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+              }
+            }
           }
+          if (ASRC == A_TMEM_DQ) tmem_wait_st();
+          else fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&afull[b]);
         }
-        if (!ok) break;
       }
-      if (kh == 0) {
-        // epilogue: accumulator lane l = weight row of this tile, columns = token rows
-        if (!warp_wait(accfull, it & 1, p, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+    }
+  } else if (warp >= kFirstEpiWarp) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int l = 32 * q + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    int it = 0;
+    for (int i = blockIdx.x; i < total; i += gridDim.x, ++it) {
+      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+      const int ab = it & 1;
+      if (!warp_wait(&accfull[ab], (it >> 1) & 1, p, abort_flag)) break;
+      tc_fence_after();
 #pragma unroll
-        for (int cb = 0; cb < NT; cb += 16) {
-          uint32_t v[16];
-          __syncwarp();
-          tmem_ld16(lane_base + C::kAccCol + cb, v);
-          tmem_wait_ld();
-          if (OP == MOE_GEMM_GATEUP_SILU) {
-            float u[16];
+      for (int cb = 0; cb < NT; cb += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld16(lane_base + C::kAccCol + ab * NT + cb, v);
+        tmem_wait_ld();
+        if (OP == MOE_GEMM_GATEUP_SILU) {
+          float u[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) u[c] = __shfl_down_sync(0xFFFFFFFFu, __uint_as_float(v[c]), 16);
-            const int j = ti.wt * 64 + 16 * q + lane;
-            if (lane < 16 && j < p.out_cols) {
+          for (int c = 0; c < 16; ++c) u[c] = __shfl_down_sync(0xFFFFFFFFu, __uint_as_float(v[c]), 16);
+          const int j = ti.wt * 64 + 16 * q + lane;
+          if (lane < 16 && j < p.out_cols) {
+            const int col = p.out_mma_order ? mma_order_pos(j) : j;
 #pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const int row = ti.row0 + cb + c;
-                if (cb + c < ti.nvalid && row < p.R) {
-                  const float gt = __uint_as_float(v[c]);
-                  const float h = gt / (1.0f + __expf(-gt)) * u[c];
-                  p.out[static_cast<int64_t>(row) * p.out_cols + j] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
-                }
-              }
-            }
-          } else {
-            const int n = ti.wt * BM + l;
-            if (n < p.out_cols) {
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const int row = ti.row0 + cb + c;
-                if (cb + c < ti.nvalid && row < p.R)
-                  p.out[static_cast<int64_t>(row) * p.out_cols + n] =
-                      __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
+            for (int c = 0; c < 16; ++c) {
+              const int row = ti.row0 + cb + c;
+              if (cb + c < ti.nvalid && row < p.R) {
+                const float gt = __uint_as_float(v[c]);
+                const float h = gt / (1.0f + __expf(-gt)) * u[c];
+                p.out[static_cast<int64_t>(row) * p.out_cols + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
               }
             }
           }
+        } else {
+          const int n = ti.wt * BM + l;
+          if (n < p.out_cols) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int row = ti.row0 + cb + c;
+              if (cb + c < ti.nvalid && row < p.R)
+                p.out[static_cast<int64_t>(row) * p.out_cols + n] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
+            }
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(accempty);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[ab]);
     }
   }
 
@@ -555,6 +570,8 @@ cudaError_t dispatch(const TcParams& prm, int asrc, int nt, int grid, cudaStream
 cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, cudaStream_t s) {
   if (p.R <= 0) return cudaSuccess;
   if (p.bf16_weights != (asrc == A_SMEM_BF16)) return cudaErrorNotSupported;
+  // int4 weights are dequantised in MMA K order: the token rows must be stored that way too
+  if (!p.bf16_weights && !p.a_mma_order) return cudaErrorNotSupported;
   if (!p.bf16_weights && p.E > kMaxE) return cudaErrorNotSupported;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -587,6 +604,7 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.uniform_rows = p.uniform_rows;
   prm.rows_total = static_cast<int>(rows_total);
   prm.R = p.R;
+  prm.out_mma_order = p.out_mma_order ? 1 : 0;
   prm.timeout_ns = 2000000000ull;
   // upper bound on tiles: every expert with rows contributes ceil(rows/nt) <= rows/nt + 1 chunks
   const int n_wt = (p.op == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;

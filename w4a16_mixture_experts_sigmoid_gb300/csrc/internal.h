@@ -20,8 +20,11 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
 int permute_blocks(int64_t Tk);  // number of segments of the count/scatter kernels
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* offsets, int32_t* sorted_ids,
                            int32_t* inv_perm, int32_t* hist, int* status, cudaStream_t s);
+// x_perm[row] = x[sorted_ids[row]], in natural or MMA K order (see gemm_tc.cu)
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const int32_t* offsets, int E, int R,
-                          int H, uint16_t* x_perm, cudaStream_t s);
+                          int H, bool mma_order, uint16_t* x_perm, cudaStream_t s);
+// dst = src rows (natural order) rewritten in MMA K order
+cudaError_t launch_to_mma_order(const uint16_t* src, uint16_t* dst, int64_t rows, int K, cudaStream_t s);
 
 // combine
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
@@ -43,6 +46,8 @@ struct GemmProblem {
   int out_cols;            // I (gate/up) or H (down)
   int R;                   // rows of a and out
   int uniform_rows;        // >= 0: a single group of that many rows
+  bool a_mma_order;        // rows of a are stored in MMA K order
+  bool out_mma_order;      // gate/up: write h in MMA K order
 };
 
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t s);

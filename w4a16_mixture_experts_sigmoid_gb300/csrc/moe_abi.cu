@@ -118,9 +118,12 @@ int auto_tokens_per_tile(int64_t rows, int groups) {
   return 128;
 }
 
+// One grouped GEMM. rows_mma_order: a (and, for gate/up, out) are stored in
+// the tensor-core K order. The tensor-core kernel needs its token rows in that
+// order; natural-order rows are first rewritten into `scratch` (R * K * 2 bytes).
 moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights_t* w, const uint16_t* a,
                               int32_t T, const int32_t* offsets, uint16_t* out, int* status, uint32_t flags,
-                              int sms, cudaStream_t s) {
+                              bool rows_mma_order, uint16_t* scratch, int sms, cudaStream_t s) {
   GemmProblem p;
   p.op = op;
   p.bf16_weights = false;
@@ -131,6 +134,8 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
   p.E = d.E;
   p.R = T * d.top_k;
   p.uniform_rows = -1;
+  p.a_mma_order = rows_mma_order;
+  p.out_mma_order = rows_mma_order;
   if (op == MOE_GEMM_GATEUP_SILU) {
     p.w = w->w13_packed;
     p.scales = w->w13_scale;
@@ -151,6 +156,13 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
     nt = auto_tokens_per_tile(p.R, d.E);
     if (asrc == A_SMEM_DQ && nt > 32) nt = 32;
   }
+  if (!p.a_mma_order) {
+    if (scratch == nullptr) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const cudaError_t ec = launch_to_mma_order(a, scratch, p.R, p.K, s);
+    if (ec != cudaSuccess) return MOE_ERR_CUDA;
+    p.a = scratch;
+    p.a_mma_order = true;
+  }
   const cudaError_t e = launch_gemm_tc(p, asrc, nt, sms, s);
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(e);
@@ -167,6 +179,8 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   p.E = 1;
   p.R = T;
   p.uniform_rows = T;
+  p.a_mma_order = false;
+  p.out_mma_order = false;
   // gate/up: [T][H] -> hs [T][Is]
   p.op = MOE_GEMM_GATEUP_SILU;
   p.w = w->shared_wgu;
@@ -205,13 +219,16 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
   uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
   const int R = T * d.top_k;
+  // the tensor-core GEMMs exchange activation rows in their K order; the CUDA-core path in natural order
+  const bool mma_order = (flags & MOE_FLAG_GEMM_SIMT) == 0;
   cudaError_t e = launch_route(logits, T, d.E, d.top_k, ids, tw, s);
   if (e == cudaSuccess) e = launch_permute(ids, T, d.E, d.top_k, offsets, sorted, inv, hist, status, s);
-  if (e == cudaSuccess) e = launch_gather(x, sorted, offsets, d.E, R, d.H, xperm, s);
+  if (e == cudaSuccess) e = launch_gather(x, sorted, offsets, d.E, R, d.H, mma_order, xperm, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, sms, s);
+  moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, mma_order,
+                                     nullptr, sms, s);
   if (st != MOE_OK) return st;
-  st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags, sms, s);
+  st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags, mma_order, nullptr, sms, s);
   if (st != MOE_OK) return st;
   const uint16_t* addend = nullptr;
   if (w->shared_wgu != nullptr) {
@@ -277,7 +294,7 @@ moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, v
 
 moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t* expert_offsets,
                          int32_t* sorted_token_ids, int32_t* inv_perm, const uint16_t* x, int32_t H,
-                         uint16_t* x_perm, void* ws, size_t ws_bytes, void* stream) {
+                         uint16_t* x_perm, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -299,7 +316,8 @@ moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t 
   cudaError_t e = launch_permute(topk_ids, T, E, k, expert_offsets, sorted_token_ids, inv_perm,
                                  reinterpret_cast<int32_t*>(w8 + 256), reinterpret_cast<int*>(w8), s);
   if (e == cudaSuccess && gather)
-    e = launch_gather(x, sorted_token_ids, expert_offsets, E, static_cast<int>(Tk), H, x_perm, s);
+    e = launch_gather(x, sorted_token_ids, expert_offsets, E, static_cast<int>(Tk), H,
+                      (flags & MOE_FLAG_ROWS_MMA_ORDER) != 0, x_perm, s);
   return cuda_status(e);
 }
 
@@ -314,12 +332,17 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
   if (T == 0) return MOE_OK;
   if (a_rows == nullptr || expert_offsets == nullptr || out_rows == nullptr || ws == nullptr)
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(a_rows) || !aligned16(out_rows)) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < 256) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(a_rows) || !aligned16(out_rows) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const bool rows_mma = (flags & MOE_FLAG_ROWS_MMA_ORDER) != 0;
+  const size_t K = (op == MOE_GEMM_GATEUP_SILU) ? d.H : d.I;
+  const bool convert = !rows_mma && !(flags & MOE_FLAG_GEMM_SIMT);
+  const size_t need = 256 + (convert ? align256(static_cast<size_t>(T) * d.top_k * K * 2) : 0);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
-  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, out_rows, static_cast<int*>(ws), flags, di.sms,
-                          as_stream(stream));
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, out_rows, reinterpret_cast<int*>(w8), flags, rows_mma,
+                          convert ? reinterpret_cast<uint16_t*>(w8 + 256) : nullptr, di.sms, as_stream(stream));
 }
 
 moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* out,

@@ -127,7 +127,15 @@ __global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32
   }
 }
 
+// Eight bf16 inputs (one 16-byte chunk) from natural order to the tensor-core
+// GEMM's K order [0,4,1,5,2,6,3,7] (see gemm_tc.cu).
+__device__ __forceinline__ uint4 to_mma_order8(const uint4 v) {
+  return make_uint4(__byte_perm(v.x, v.z, 0x5410), __byte_perm(v.x, v.z, 0x7632), __byte_perm(v.y, v.w, 0x5410),
+                    __byte_perm(v.y, v.w, 0x7632));
+}
+
 // x_perm[row] = x[sorted_ids[row]] for rows < offsets[E]; 16-byte copies.
+template <bool MMA_ORDER>
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int R, int H8,
                                                      uint4* __restrict__ xp) {
@@ -135,8 +143,17 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
   for (int row = blockIdx.x; row < R && row < valid; row += gridDim.x) {
     const uint4* src = x + (int64_t)sorted_ids[row] * H8;
     uint4* dst = xp + (int64_t)row * H8;
-    for (int c = threadIdx.x; c < H8; c += blockDim.x) dst[c] = __ldg(src + c);
+    for (int c = threadIdx.x; c < H8; c += blockDim.x) {
+      const uint4 v = __ldg(src + c);
+      dst[c] = MMA_ORDER ? to_mma_order8(v) : v;
+    }
   }
+}
+
+__global__ void __launch_bounds__(256) to_mma_order_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                           int64_t n8) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = to_mma_order8(__ldg(src + i));
 }
 
 }  // namespace
@@ -156,11 +173,26 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* off
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const int32_t* offsets, int E, int R, int H,
-                          uint16_t* x_perm, cudaStream_t s) {
+                          bool mma_order, uint16_t* x_perm, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const int blocks = R < 4096 ? R : 4096;
-  gather_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
-                                       reinterpret_cast<uint4*>(x_perm));
+  if (mma_order)
+    gather_kernel<true><<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
+                                               reinterpret_cast<uint4*>(x_perm));
+  else
+    gather_kernel<false><<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
+                                                reinterpret_cast<uint4*>(x_perm));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_mma_order(const uint16_t* src, uint16_t* dst, int64_t rows, int K, cudaStream_t s) {
+  const int64_t n8 = rows * (K / 8);
+  if (n8 <= 0) return cudaSuccess;
+  int64_t blocks = (n8 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  to_mma_order_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(src),
+                                                                    reinterpret_cast<uint4*>(dst), n8);
   count_launches(1);
   return cudaGetLastError();
 }
