@@ -21,17 +21,24 @@
 // the gather writes x rows that way and the gate/up epilogue writes h that
 // way, at no extra cost.
 //
-// One persistent CTA per SM, 16 warps:
-//   warp 0      TMA producer: int4 words + bf16 scales + token rows into a
-//               ring of STAGES shared-memory stages (128-byte swizzle).
-//   warp 1      MMA issuer (one thread): tcgen05.mma, fp32 accumulators in TMEM.
-//   warp 2      owns the tensor-memory allocation; warp 3 builds the tile list.
-//   warps 4-11  dequantise, in two groups of four that take alternate stages:
+// One persistent CTA per SM, 15 warps:
+//   warp 0      builds the tile list, then is the weight producer: TMA of int4
+//               words + bf16 scales (or dense bf16 weights) into the weight ring.
+//   warp 14     token-row producer: TMA of the token rows into their ring; a
+//               warp of its own so that the weight stream never waits on it.
+//   warps 1, 15 MMA issuers (lane 0 each; warp 1 also owns the tensor-memory
+//               allocation). A thread can issue one M=128 MMA about every 45
+//               cycles whatever N is, while the tensor core accepts MMAs from
+//               several threads at once; so each of the two dequant groups
+//               has its own issuer and its own fp32 accumulators, and the
+//               epilogue adds the two. (With 128 tokens per tile one issuer
+//               keeps up with the math, and tensor memory holds one set.)
+//   warps 2-9   dequantise, in two groups of four that take alternate stages:
 //               each thread owns one weight row (= one TMEM lane) of its
 //               group's stage and turns its 256 nibbles into bf16(q*s) in the
 //               MMA's A operand: tensor memory (default) or swizzled shared
 //               memory (MOE_FLAG_A_SMEM).
-//   warps 12-15 epilogue: TMEM -> registers -> SiLU(gate)*up (gate/up) or the
+//   warps 10-13 epilogue: TMEM -> registers -> SiLU(gate)*up (gate/up) or the
 //               plain row (down) -> bf16 rows in global memory. Accumulators
 //               are double-buffered, so the epilogue of one tile overlaps the
 //               MMAs of the next.
@@ -60,9 +67,11 @@ constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BK = 256;            // K per pipeline stage
 constexpr int KSUB = 64;           // K per 128-byte swizzle row
 constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
-constexpr int kThreads = 512;
-constexpr int kFirstDqWarp = 4;
-constexpr int kFirstEpiWarp = 12;
+constexpr int kThreads = 512;      // 16 warps, 128 registers a thread
+constexpr int kFirstDqWarp = 2;
+constexpr int kFirstEpiWarp = 10;
+constexpr int kBProducerWarp = 14;
+constexpr int kSecondMmaWarp = 15;
 constexpr int kMaxE = 1024;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_100-class parts
 constexpr int kAlignSlack = 1024;
@@ -80,25 +89,38 @@ struct TcParams {
   unsigned long long timeout_ns;
 };
 
+// Shared memory holds two rings. The weight ring (int4 words + scales, or
+// dense bf16 weights) is released by the dequant warps as soon as they have
+// the stage in registers, so HBM streaming never waits on the tensor pipe; the
+// token-row ring (operand B) is released by the MMA commit. With dense bf16
+// weights the MMA reads both, and the two rings advance in lock step.
 template <int ASRC, int NT>
 struct Cfg {
-  static constexpr int kAStage = (ASRC == A_SMEM_BF16) ? NSUB * BM * 128 : BM * 128;
+  static constexpr bool kDq = ASRC != A_SMEM_BF16;
+  static constexpr int kAStage = kDq ? BM * 128 : NSUB * BM * 128;
+  static constexpr int kSStage = kDq ? BM * 16 : 0;
+  static constexpr int kWStage = kAStage + kSStage;
   static constexpr int kBStage = NSUB * NT * 128;
-  static constexpr int kSStage = (ASRC == A_SMEM_BF16) ? 0 : BM * 16;
-  static constexpr int kStage = kAStage + kBStage + kSStage;
-  static constexpr int kNBuf = (ASRC == A_TMEM_DQ) ? (NT <= 64 ? 3 : 2) : (ASRC == A_SMEM_DQ ? 2 : 1);
+  static constexpr int kNBuf = (ASRC == A_TMEM_DQ) ? (NT <= 32 ? 3 : 2) : (ASRC == A_SMEM_DQ ? 2 : 1);
   static constexpr int kABuf = (ASRC == A_SMEM_DQ) ? NSUB * BM * 128 : 0;
   static constexpr int kAvail = kSmemLimit - kAlignSlack - kAuxBytes - (ASRC == A_SMEM_DQ ? kNBuf * kABuf : 0);
-  static constexpr int kStagesRaw = kAvail / kStage;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kBFit = (kAvail - 3 * kWStage) / kBStage;
+  static constexpr int kBStagesDq = (kNBuf + 3 < kBFit ? kNBuf + 3 : kBFit);
+  static constexpr int kWStagesDq = (kAvail - kBStagesDq * kBStage) / kWStage;
+  static constexpr int kLock = kAvail / (kWStage + kBStage);
+  static constexpr int kWStages = kDq ? (kWStagesDq > 12 ? 12 : kWStagesDq) : (kLock > 8 ? 8 : kLock);
+  static constexpr int kBStages = kDq ? kBStagesDq : kWStages;
+  static constexpr int kMmaGroups = NT <= 64 ? 2 : 1;   // MMA issuers, each with its own accumulators
   static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
-  static constexpr int kColsNeeded = kAccCol + 2 * NT;   // two accumulators
+  static constexpr int kColsNeeded = kAccCol + 2 * kMmaGroups * NT;   // double-buffered per issuer
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
                                    : kColsNeeded <= 256 ? 256 : 512;
-  static constexpr int kSmemBytes = kAlignSlack + kStages * kStage + kNBuf * kABuf + kAuxBytes;
-  static_assert(kStages >= 2, "pipeline needs at least two stages");
+  static constexpr int kSmemBytes =
+      kAlignSlack + kWStages * kWStage + kBStages * kBStage + kNBuf * kABuf + kAuxBytes;
+  static_assert(kWStages >= 2 && kBStages >= 2, "each ring needs at least two stages");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
   static_assert(kColsNeeded <= 512, "tensor memory overflow");
-  static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
 struct TileInfo {
@@ -166,15 +188,19 @@ __device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3)
 template <int OP, int ASRC, int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<ASRC, NT>;
-  constexpr int S = C::kStages;
+  constexpr int SW = C::kWStages;
+  constexpr int SB = C::kBStages;
   constexpr int NB = C::kNBuf;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* abuf = smem + S * C::kStage;
+  uint8_t* bring = smem + SW * C::kWStage;
+  uint8_t* abuf = bring + SB * C::kBStage;
   uint8_t* aux = abuf + NB * C::kABuf;
-  uint64_t* full = reinterpret_cast<uint64_t*>(aux);
-  uint64_t* empty = full + S;
-  uint64_t* afull = empty + S;
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(aux);
+  uint64_t* wempty = wfull + SW;
+  uint64_t* bfull = wempty + SW;
+  uint64_t* bempty = bfull + SB;
+  uint64_t* afull = bempty + SB;
   uint64_t* aempty = afull + NB;
   uint64_t* accfull = aempty + NB;   // [2]
   uint64_t* accempty = accfull + 2;  // [2]
@@ -190,15 +216,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) { mbar_init(&full[s], 32); mbar_init(&empty[s], 1); }
+    for (int s = 0; s < SW; ++s) { mbar_init(&wfull[s], 32); mbar_init(&wempty[s], C::kDq ? 4 : 1); }
+    for (int s = 0; s < SB; ++s) { mbar_init(&bfull[s], 1); mbar_init(&bempty[s], 1); }
     for (int b = 0; b < NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], 1); mbar_init(&accempty[a], 4); }
-    mbar_init(drain, 1);
+    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], C::kMmaGroups); mbar_init(&accempty[a], 4); }
+    mbar_init(drain, C::kMmaGroups);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 2) tmem_alloc(tmem_slot, C::kTmemCols);
-  if (warp == 3) {
+  if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
+  if (warp == 0) {
     // compact list of experts with rows, and the prefix of their tile counts
     if (p.uniform_rows >= 0) {
       if (lane == 0) {
@@ -246,10 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = l2_policy_evict_first();
-    const uint64_t pol_b = l2_policy_evict_last();
-    constexpr uint32_t kTx = (ASRC == A_SMEM_BF16) ? (NSUB * BM * 128 + NSUB * NT * 128)
-                                                   : (BM * 128 + NSUB * NT * 128);
-    const uint32_t tx = kTx + ((ASRC != A_SMEM_BF16 && p.scale_tma) ? BM * 16 : 0);
+    const uint32_t txw = C::kAStage + ((C::kDq && p.scale_tma) ? BM * 16 : 0);
     const int kg = p.K / 32;
     int g = 0;
     bool ok = true;
@@ -260,13 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (OP == MOE_GEMM_GATEUP_SILU) { grow_lo = ebase + ti.wt * 64; grow_hi = ebase + p.out_cols + ti.wt * 64; }
       else { grow_lo = ebase + ti.wt * BM; grow_hi = grow_lo + 64; }
       for (int ks = 0; ks < nk; ++ks, ++g) {
-        const int s = g % S;
-        const uint32_t ph = (g / S) & 1;
-        if (!warp_wait(&empty[s], ph ^ 1, p, abort_flag)) { ok = false; break; }
-        uint8_t* sa = smem + s * C::kStage;
-        uint8_t* sb = sa + C::kAStage;
-        uint8_t* ss = sb + C::kBStage;
-        if (ASRC != A_SMEM_BF16 && !p.scale_tma) {
+        const int sw = g % SW;
+        if (!warp_wait(&wempty[sw], ((g / SW) & 1) ^ 1, p, abort_flag)) { ok = false; break; }
+        uint8_t* sa = smem + sw * C::kWStage;
+        uint8_t* ss = sa + C::kAStage;
+        if (C::kDq && !p.scale_tma) {
           // scales by plain loads (row stride not 16-byte aligned): lane owns rows lane + 32 r
           uint16_t* sc = reinterpret_cast<uint16_t*>(ss);
           for (int r = lane; r < BM; r += 32) {
@@ -281,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], tx);
-          if (ASRC == A_SMEM_BF16) {
+          mbar_arrive_expect_tx(&wfull[sw], txw);
+          if (!C::kDq) {
 #pragma unroll
             for (int sub = 0; sub < NSUB; ++sub) {
 #pragma unroll
@@ -290,62 +312,88 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 int grow;
                 if (OP == MOE_GEMM_GATEUP_SILU) grow = (rb & 1) * p.out_cols + ti.wt * 64 + 16 * (rb >> 1);
                 else grow = ti.wt * BM + 16 * rb;
-                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, &full[s], ks * BK + sub * KSUB, grow, pol_w);
+                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, &wfull[sw], ks * BK + sub * KSUB, grow,
+                            pol_w);
               }
             }
           } else {
-            tma_load_2d(sa, &p.tm_w, &full[s], ks * (BK / 8), grow_lo, pol_w);
-            tma_load_2d(sa + 64 * 128, &p.tm_w, &full[s], ks * (BK / 8), grow_hi, pol_w);
+            tma_load_2d(sa, &p.tm_w, &wfull[sw], ks * (BK / 8), grow_lo, pol_w);
+            tma_load_2d(sa + 64 * 128, &p.tm_w, &wfull[sw], ks * (BK / 8), grow_hi, pol_w);
             if (p.scale_tma) {
-              tma_load_2d(ss, &p.tm_s, &full[s], ks * 8, grow_lo, pol_w);
-              tma_load_2d(ss + 64 * 16, &p.tm_s, &full[s], ks * 8, grow_hi, pol_w);
+              tma_load_2d(ss, &p.tm_s, &wfull[sw], ks * 8, grow_lo, pol_w);
+              tma_load_2d(ss + 64 * 16, &p.tm_s, &wfull[sw], ks * 8, grow_hi, pol_w);
             }
           }
-#pragma unroll
-          for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, &full[s], ks * BK + sub * KSUB, ti.row0, pol_b);
         } else {
-          mbar_arrive(&full[s]);
+          mbar_arrive(&wfull[sw]);
         }
       }
     }
     // let every copy issued into this CTA's shared memory land before exit
     if (lane == 0) {
-      for (int d = 0; d < S && d < g; ++d) {
+      for (int d = 0; d < SW && d < g; ++d) {
         const int gg = g - 1 - d;
-        mbar_wait(&full[gg % S], (gg / S) & 1, p.timeout_ns, nullptr, p.status);
+        mbar_wait(&wfull[gg % SW], (gg / SW) & 1, p.timeout_ns, nullptr, p.status);
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kBProducerWarp) {
+    // ------------------------------------------------------------ token-row producer (one lane)
+    if (lane == 0) {
+      const uint64_t pol_b = l2_policy_evict_last();
+      constexpr uint32_t txb = NSUB * NT * 128;
+      int g = 0;
+      bool ok = true;
+      for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
+        const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          const int sbi = g % SB;
+          if (!mbar_wait(&bempty[sbi], ((g / SB) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sb = bring + sbi * C::kBStage;
+          mbar_arrive_expect_tx(&bfull[sbi], txb);
+#pragma unroll
+          for (int sub = 0; sub < NSUB; ++sub)
+            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, &bfull[sbi], ks * BK + sub * KSUB, ti.row0, pol_b);
+        }
+      }
+      for (int d = 0; d < SB && d < g; ++d) {
+        const int gg = g - 1 - d;
+        mbar_wait(&bfull[gg % SB], (gg / SB) & 1, p.timeout_ns, nullptr, p.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 || (C::kMmaGroups == 2 && warp == kSecondMmaWarp)) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, NT);
+      const int mg = (warp == 1) ? 0 : 1;  // with two issuers, issuer mg takes the stages g with g % 2 == mg
       int g = 0, it = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
         const int ab = it & 1;
         if (!mbar_wait(&accempty[ab], ((it >> 1) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + C::kAccCol + ab * NT;
+        const uint32_t d_tmem = tmem + C::kAccCol + (mg * 2 + ab) * NT;
+        bool first = true;
         for (int ks = 0; ks < nk; ++ks, ++g) {
-          const int s = g % S;
-          const uint32_t ph = (g / S) & 1;
+          if (C::kMmaGroups == 2 && (g & 1) != mg) continue;
+          const int sw = g % SW, sbi = g % SB;
           const int b = g % NB;
-          const uint32_t pha = (g / NB) & 1;
-          if (!mbar_wait(&full[s], ph, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
-          if (ASRC != A_SMEM_BF16) {
-            if (!mbar_wait(&afull[b], pha, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&bfull[sbi], (g / SB) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          if (C::kDq) {
+            if (!mbar_wait(&afull[b], (g / NB) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          } else {
+            if (!mbar_wait(&wfull[sw], (g / SW) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * C::kStage);
-          const uint32_t sb = sa + C::kAStage;
+          const uint32_t sa = smem_u32(smem + sw * C::kWStage);
+          const uint32_t sb = smem_u32(bring + sbi * C::kBStage);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const int sub = kk >> 2;
             const uint32_t koff = (kk & 3) * 32;
             const uint64_t bdesc = sw128_kmajor_desc(sb + sub * (NT * 128) + koff);
-            const uint32_t acc = (ks > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
             if (ASRC == A_TMEM_DQ) {
               mma_ts(d_tmem, tmem + b * 128 + kk * 8, bdesc, idesc, acc);
             } else if (ASRC == A_SMEM_DQ) {
@@ -356,11 +404,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               mma_ss(d_tmem, adesc, bdesc, idesc, acc);
             }
           }
-          mma_commit(&empty[s]);
-          if (ASRC != A_SMEM_BF16) mma_commit(&aempty[b]);
+          first = false;
+          mma_commit(&bempty[sbi]);
+          if (C::kDq) mma_commit(&aempty[b]);
+          else mma_commit(&wempty[sw]);
         }
         if (!ok) break;
-        mma_commit(&accfull[ab]);
+        mma_commit(&accfull[ab]);   // an issuer with no stage in this tile arrives at once
       }
       // let every MMA issued by this thread finish before tensor memory is freed
       mma_commit(drain);
@@ -371,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ------------------------------------------------------------ dequantise
     if (ASRC != A_SMEM_BF16) {
       const int grp = (warp - kFirstDqWarp) >> 2;  // takes the stages g with g % 2 == grp
-      const int q = warp & 3;                      // TMEM lane quarter this warp may access
+      const int q = warp & 3;                      // TMEM lane quarter this warp may access (warp id mod 4)
       const int l = 32 * q + lane;
       const int r_sm = (OP == MOE_GEMM_GATEUP_SILU) ? (lane < 16 ? 16 * q + lane : 64 + 16 * q + (lane - 16)) : l;
       const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
@@ -380,14 +430,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
         for (int ks = 0; ks < nk; ++ks, ++g) {
           if ((g & 1) != grp) continue;
-          const int s = g % S;
-          const uint32_t ph = (g / S) & 1;
+          const int sw = g % SW;
           const int b = g % NB;
           const uint32_t pha = (g / NB) & 1;
-          if (!warp_wait(&full[s], ph, p, abort_flag)) { ok = false; break; }
-          const uint8_t* arow = smem + s * C::kStage + r_sm * 128;
-          const uint4 sv = *reinterpret_cast<const uint4*>(smem + s * C::kStage + C::kAStage + C::kBStage + r_sm * 16);
-          const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
+          if (!warp_wait(&wfull[sw], (g / SW) & 1, p, abort_flag)) { ok = false; break; }
+          // the stage row comes into registers in two halves of four 16-byte chunks; once the
+          // second half is loaded the stage goes back to the producer
+          const uint8_t* arow = smem + sw * C::kWStage + r_sm * 128;
+          const uint4 sv = *reinterpret_cast<const uint4*>(smem + sw * C::kWStage + C::kAStage + r_sm * 16);
+          const uint32_t sw4[4] = {sv.x, sv.y, sv.z, sv.w};
           uint4 wv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
@@ -399,12 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 wv[c] = *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&wempty[sw]);
             }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
               const int c = half * 4 + cc;
               uint32_t dq[16];
-              dequant_group(wv[cc], (c & 1) ? (sw[c >> 1] >> 16) : (sw[c >> 1] & 0xFFFFu), dq);
+              dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dq);
               if (ASRC == A_TMEM_DQ) {
                 tmem_st16(lane_base + b * 128 + c * 16, dq);
               } else {
@@ -424,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
       }
     }
-  } else if (warp >= kFirstEpiWarp) {
+  } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const int l = 32 * q + lane;
@@ -435,12 +488,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const int ab = it & 1;
       if (!warp_wait(&accfull[ab], (it >> 1) & 1, p, abort_flag)) break;
       tc_fence_after();
+      // which issuers accumulated into this tile: with one stage per tile only the one whose parity it has
+      const int g0 = it * nk;
+      const bool use0 = C::kMmaGroups == 1 || nk >= 2 || (g0 & 1) == 0;
+      const bool use1 = C::kMmaGroups == 2 && (nk >= 2 || (g0 & 1) == 1);
 #pragma unroll
       for (int cb = 0; cb < NT; cb += 16) {
         uint32_t v[16];
         __syncwarp();
-        tmem_ld16(lane_base + C::kAccCol + ab * NT + cb, v);
-        tmem_wait_ld();
+        if (use0) {
+          tmem_ld16(lane_base + C::kAccCol + ab * NT + cb, v);
+          tmem_wait_ld();
+        }
+        if (use1) {
+          uint32_t v1[16];
+          tmem_ld16(lane_base + C::kAccCol + (2 + ab) * NT + cb, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
+        }
         if (OP == MOE_GEMM_GATEUP_SILU) {
           float u[16];
 #pragma unroll
@@ -453,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               const int row = ti.row0 + cb + c;
               if (cb + c < ti.nvalid && row < p.R) {
                 const float gt = __uint_as_float(v[c]);
-                const float h = gt / (1.0f + __expf(-gt)) * u[c];
+                const float h = __fdividef(gt, 1.0f + __expf(-gt)) * u[c];  // SiLU(g) * u, rounded to bf16 below
                 p.out[static_cast<int64_t>(row) * p.out_cols + col] = __bfloat16_as_ushort(__float2bfloat16_rn(h));
               }
             }
@@ -480,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 2) tmem_dealloc(tmem, C::kTmemCols);
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
