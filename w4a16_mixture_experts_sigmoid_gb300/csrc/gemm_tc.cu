@@ -110,6 +110,14 @@ struct Cfg {
   static constexpr int kLock = kAvail / (kWStage + kBStage);
   static constexpr int kWStages = kDq ? (kWStagesDq > 12 ? 12 : kWStagesDq) : (kLock > 8 ? 8 : kLock);
   static constexpr int kBStages = kDq ? kBStagesDq : kWStages;
+  // try_wait.parity cannot tell phase k from phase k+2, so a barrier may be waited on only by a
+  // consumer that cannot run two phases ahead of it. Stages alternate between two consumers
+  // (dequant groups, MMA issuers) by g % 2, so every "full" barrier and every A-buffer barrier
+  // is kept per (g % 2, slot): the stages that share one are lcm(2, ring) apart and are all
+  // taken by one consumer in order.
+  static constexpr int kWPeriod = (kWStages % 2 == 0) ? kWStages : 2 * kWStages;
+  static constexpr int kBPeriod = (kBStages % 2 == 0) ? kBStages : 2 * kBStages;
+  static constexpr int kAPeriod = (kNBuf % 2 == 0) ? kNBuf : 2 * kNBuf;
   static constexpr int kMmaGroups = NT <= 64 ? 2 : 1;   // MMA issuers, each with its own accumulators
   static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
   static constexpr int kColsNeeded = kAccCol + 2 * kMmaGroups * NT;   // double-buffered per issuer
@@ -119,6 +127,8 @@ struct Cfg {
       kAlignSlack + kWStages * kWStage + kBStages * kBStage + kNBuf * kABuf + kAuxBytes;
   static_assert(kWStages >= 2 && kBStages >= 2, "each ring needs at least two stages");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
+  static_assert(8 * (3 * kWStages + 3 * kBStages + 4 * kNBuf + 5) + 16 + 2 * kMaxE + 4 * (kMaxE + 1) <= kAuxBytes,
+                "barriers and tile table overflow the aux area");
   static_assert(kColsNeeded <= 512, "tensor memory overflow");
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
@@ -182,6 +192,15 @@ __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bi
   }
 }
 
+// A buffer b is reused every NB stages and the stages alternate between two dequant groups, so
+// its barriers are kept per (g % 2, b); the stages sharing one are P = lcm(2, NB) apart and g / P
+// counts the earlier ones. Buffer b is handed from stage g to stage g + NB: stage g waits for as
+// many releases of its (group, buffer) pair as there are stages g' <= g in its class mod P with
+// g' >= NB.
+__device__ __forceinline__ int a_releases_needed(int g, int nb, int period) {
+  return g / period + (g % period >= nb ? 1 : 0);
+}
+
 // position of input j inside its block of 8 when a row is stored in MMA order
 __device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1); }
 
@@ -196,13 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint8_t* bring = smem + SW * C::kWStage;
   uint8_t* abuf = bring + SB * C::kBStage;
   uint8_t* aux = abuf + NB * C::kABuf;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(aux);
-  uint64_t* wempty = wfull + SW;
-  uint64_t* bfull = wempty + SW;
-  uint64_t* bempty = bfull + SB;
-  uint64_t* afull = bempty + SB;
-  uint64_t* aempty = afull + NB;
-  uint64_t* accfull = aempty + NB;   // [2]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(aux);   // [2][SW]: (stage parity, slot)
+  uint64_t* wempty = wfull + 2 * SW;
+  uint64_t* bfull = wempty + SW;                         // [2][SB]
+  uint64_t* bempty = bfull + 2 * SB;
+  uint64_t* afull = bempty + SB;      // [2][NB]: (dequant group, A buffer)
+  uint64_t* aempty = afull + 2 * NB;  // [2][NB]
+  uint64_t* accfull = aempty + 2 * NB;   // [2]
   uint64_t* accempty = accfull + 2;  // [2]
   uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -216,9 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SW; ++s) { mbar_init(&wfull[s], 32); mbar_init(&wempty[s], C::kDq ? 4 : 1); }
-    for (int s = 0; s < SB; ++s) { mbar_init(&bfull[s], 1); mbar_init(&bempty[s], 1); }
-    for (int b = 0; b < NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
+    for (int s = 0; s < 2 * SW; ++s) mbar_init(&wfull[s], 32);
+    for (int s = 0; s < SW; ++s) mbar_init(&wempty[s], C::kDq ? 4 : 1);
+    for (int s = 0; s < 2 * SB; ++s) mbar_init(&bfull[s], 1);
+    for (int s = 0; s < SB; ++s) mbar_init(&bempty[s], 1);
+    for (int b = 0; b < 2 * NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], C::kMmaGroups); mbar_init(&accempty[a], 4); }
     mbar_init(drain, C::kMmaGroups);
     *abort_flag = 0;
@@ -285,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       else { grow_lo = ebase + ti.wt * BM; grow_hi = grow_lo + 64; }
       for (int ks = 0; ks < nk; ++ks, ++g) {
         const int sw = g % SW;
+        uint64_t* wf = &wfull[(g & 1) * SW + sw];
         if (!warp_wait(&wempty[sw], ((g / SW) & 1) ^ 1, p, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + sw * C::kWStage;
         uint8_t* ss = sa + C::kAStage;
@@ -303,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&wfull[sw], txw);
+          mbar_arrive_expect_tx(wf, txw);
           if (!C::kDq) {
 #pragma unroll
             for (int sub = 0; sub < NSUB; ++sub) {
@@ -312,20 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 int grow;
                 if (OP == MOE_GEMM_GATEUP_SILU) grow = (rb & 1) * p.out_cols + ti.wt * 64 + 16 * (rb >> 1);
                 else grow = ti.wt * BM + 16 * rb;
-                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, &wfull[sw], ks * BK + sub * KSUB, grow,
+                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, wf, ks * BK + sub * KSUB, grow,
                             pol_w);
               }
             }
           } else {
-            tma_load_2d(sa, &p.tm_w, &wfull[sw], ks * (BK / 8), grow_lo, pol_w);
-            tma_load_2d(sa + 64 * 128, &p.tm_w, &wfull[sw], ks * (BK / 8), grow_hi, pol_w);
+            tma_load_2d(sa, &p.tm_w, wf, ks * (BK / 8), grow_lo, pol_w);
+            tma_load_2d(sa + 64 * 128, &p.tm_w, wf, ks * (BK / 8), grow_hi, pol_w);
             if (p.scale_tma) {
-              tma_load_2d(ss, &p.tm_s, &wfull[sw], ks * 8, grow_lo, pol_w);
-              tma_load_2d(ss + 64 * 16, &p.tm_s, &wfull[sw], ks * 8, grow_hi, pol_w);
+              tma_load_2d(ss, &p.tm_s, wf, ks * 8, grow_lo, pol_w);
+              tma_load_2d(ss + 64 * 16, &p.tm_s, wf, ks * 8, grow_hi, pol_w);
             }
           }
         } else {
-          mbar_arrive(&wfull[sw]);
+          mbar_arrive(wf);
         }
       }
     }
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     if (lane == 0) {
       for (int d = 0; d < SW && d < g; ++d) {
         const int gg = g - 1 - d;
-        mbar_wait(&wfull[gg % SW], (gg / SW) & 1, p.timeout_ns, nullptr, p.status);
+        mbar_wait(&wfull[(gg & 1) * SW + gg % SW], (gg / C::kWPeriod) & 1, p.timeout_ns, nullptr, p.status);
       }
     }
     __syncwarp();
@@ -350,15 +372,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const int sbi = g % SB;
           if (!mbar_wait(&bempty[sbi], ((g / SB) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sb = bring + sbi * C::kBStage;
-          mbar_arrive_expect_tx(&bfull[sbi], txb);
+          uint64_t* bf = &bfull[(g & 1) * SB + sbi];
+          mbar_arrive_expect_tx(bf, txb);
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, &bfull[sbi], ks * BK + sub * KSUB, ti.row0, pol_b);
+            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, bf, ks * BK + sub * KSUB, ti.row0, pol_b);
         }
       }
       for (int d = 0; d < SB && d < g; ++d) {
         const int gg = g - 1 - d;
-        mbar_wait(&bfull[gg % SB], (gg / SB) & 1, p.timeout_ns, nullptr, p.status);
+        mbar_wait(&bfull[(gg & 1) * SB + gg % SB], (gg / C::kBPeriod) & 1, p.timeout_ns, nullptr, p.status);
       }
     }
     __syncwarp();
@@ -379,11 +402,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (C::kMmaGroups == 2 && (g & 1) != mg) continue;
           const int sw = g % SW, sbi = g % SB;
           const int b = g % NB;
-          if (!mbar_wait(&bfull[sbi], (g / SB) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          if (!mbar_wait(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           if (C::kDq) {
-            if (!mbar_wait(&afull[b], (g / NB) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
           } else {
-            if (!mbar_wait(&wfull[sw], (g / SW) & 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+            if (!mbar_wait(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + sw * C::kWStage);
@@ -406,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
           first = false;
           mma_commit(&bempty[sbi]);
-          if (C::kDq) mma_commit(&aempty[b]);
+          if (C::kDq) mma_commit(&aempty[((g + NB) & 1) * NB + b]);   // to the group of the next user
           else mma_commit(&wempty[sw]);
         }
         if (!ok) break;
@@ -432,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if ((g & 1) != grp) continue;
           const int sw = g % SW;
           const int b = g % NB;
-          const uint32_t pha = (g / NB) & 1;
-          if (!warp_wait(&wfull[sw], (g / SW) & 1, p, abort_flag)) { ok = false; break; }
+          const int a_need = a_releases_needed(g, NB, C::kAPeriod);
+          if (!warp_wait(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p, abort_flag)) { ok = false; break; }
           // the stage row comes into registers in two halves of four 16-byte chunks; once the
           // second half is loaded the stage goes back to the producer
           const uint8_t* arow = smem + sw * C::kWStage + r_sm * 128;
@@ -442,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           uint4 wv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
-          if (!warp_wait(&aempty[b], pha ^ 1, p, abort_flag)) { ok = false; break; }
+          if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -473,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           else fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[b]);
+          if (lane == 0) mbar_arrive(&afull[grp * NB + b]);
         }
       }
     }
