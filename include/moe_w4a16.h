@@ -154,6 +154,41 @@ MOE_API moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, 
                          const uint16_t* x, int32_t H, uint16_t* x_perm,
                          void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* moe_permute for callers that have no device memory to give and may not
+ * allocate any: a hook inside an engine that reserved all of HBM for its own
+ * pool, or a latency-critical path where cudaMalloc/cudaFree (which can
+ * synchronise the device) are not allowed. The pages describing the method
+ * have no counterpart of this call; it exists only for such callers.
+ *
+ * Same arguments, results and rules as moe_permute, except that the
+ * histograms come from a fixed array of MOE_PERMUTE_STATIC_SCRATCH_BYTES of
+ * device memory inside the library image (loaded once on every device that
+ * uses it, held until the process exits) and no workspace is passed. The call
+ * allocates nothing. It returns MOE_ERR_WORKSPACE_TOO_SMALL when the
+ * histograms, 4 * E * ceil(T*k / 4096) bytes, would exceed that array (with
+ * E = 384, T*k up to 2,793,472 fits; with E = 1024, up to 1,048,576).
+ *
+ * status: a caller-owned device int32 that must be 0 before the first call;
+ * an id outside [0, E) sets MOE_ERR_DEVICE_BOUNDS in it (read and reset it
+ * with moe_check_status(status, stream)). May be NULL: such ids are then
+ * still left out (inv_perm entry -1) but not reported. Nothing in the
+ * library's own array has to start at zero.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the
+ * array's device address (this can load the library's module onto the
+ * device) and checks the device; make that first call before any stream
+ * capture. Later calls on the device only launch kernels.
+ *
+ * Every call on a device uses the same array: calls whose kernels overlap on
+ * the GPU (other streams, other host threads, without ordering between them)
+ * race and give wrong results. Calls on one stream are ordered and safe. */
+#define MOE_PERMUTE_STATIC_SCRATCH_BYTES (1u << 20)
+MOE_API moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k,
+                                        int32_t* expert_offsets, int32_t* sorted_token_ids,
+                                        int32_t* inv_perm, const uint16_t* x, int32_t H,
+                                        uint16_t* x_perm, int32_t* status, uint32_t flags,
+                                        void* stream);
+
 /* Steps 3 and 4, the grouped W4A16 GEMMs over expert-sorted rows. Row r of
  * a_rows (bf16 [R][K], R = T*k) belongs to the expert e with
  * expert_offsets[e] <= r < expert_offsets[e+1]. Each weight is dequantised as

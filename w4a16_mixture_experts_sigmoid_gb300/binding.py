@@ -29,6 +29,7 @@ MOE_GEMM_DOWN = 1
 MOE_FLAG_GEMM_SIMT = 0x1
 MOE_FLAG_A_SMEM = 0x2
 MOE_FLAG_ROWS_MMA_ORDER = 0x4
+MOE_PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 def MOE_FLAG_TOKENS_PER_TILE(n: int) -> int:
@@ -53,6 +54,8 @@ SIGNATURES = {
     "moe_sigmoid_scores": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_permute_static_scratch": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_int32, c_void_p, c_void_p, c_uint32, c_void_p]),
     "moe_w4a16_grouped_gemm": (c_int32, [c_int32, moe_dims_t, POINTER(moe_weights_t), c_void_p, c_int32,
                                          c_void_p, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_shared_expert": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_int32, c_void_p,
@@ -171,6 +174,14 @@ def moe_permute(topk_ids, T: int, E: int, k: int, expert_offsets, sorted_token_i
     _check(load().moe_permute(_dptr(topk_ids), T, E, k, _dptr(expert_offsets), _dptr(sorted_token_ids),
                               _dptr(inv_perm), _dptr(x), H, _dptr(x_perm), _dptr(ws), _nbytes(ws), flags,
                               _stream(stream)), "moe_permute")
+
+
+def moe_permute_static_scratch(topk_ids, T: int, E: int, k: int, expert_offsets, sorted_token_ids, inv_perm, x,
+                               H: int, x_perm, status, flags: int = 0, stream=None) -> None:
+    """moe_permute with the library's own fixed histogram scratch: no workspace, nothing allocated."""
+    _check(load().moe_permute_static_scratch(_dptr(topk_ids), T, E, k, _dptr(expert_offsets),
+                                             _dptr(sorted_token_ids), _dptr(inv_perm), _dptr(x), H, _dptr(x_perm),
+                                             _dptr(status), flags, _stream(stream)), "moe_permute_static_scratch")
 
 
 def moe_w4a16_grouped_gemm(op: int, d: moe_dims_t, w: moe_weights_t, a_rows, T: int, expert_offsets, out_rows,
