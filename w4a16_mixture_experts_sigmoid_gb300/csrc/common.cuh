@@ -192,6 +192,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// 8 columns of the thread's lane (same layout as tmem_st16, half the width). Two
+// of these per 16 columns cost fewer issue slots than one x16 store.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 operand tile stored in the
 // 128-byte swizzled layout: rows of 128 bytes (64 bf16 along K), eight rows
 // forming a 1024-byte swizzle atom (16-byte chunk c of row r stored at chunk

@@ -172,22 +172,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
 // 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
-// 8i+m (low half) and 8i+m+4 (high half) of the chunk.
+// 8i+m (low half) and 8i+m+4 (high half) of the chunk. Per pair of weights:
+// one lop3 makes the bf16 pattern 0x43<nibble> = 128 + nibble exactly, one
+// packed subtract of 136 gives q = nibble - 8 exactly, one packed multiply
+// rounds q*s once to nearest even. Written as PTX: the same two packed bf16
+// operations through the cuda_bf16 intrinsics take more issue slots.
 __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bits, uint32_t* out16) {
-  const __nv_bfloat162 s2 = __halves2bfloat162(__ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)),
-                                               __ushort_as_bfloat16(static_cast<unsigned short>(scale_bits)));
-  const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);  // 128 (magic exponent) + 8 (nibble bias)
+  const uint32_t s2 = (scale_bits & 0xFFFFu) * 0x10001u;  // the scale in both halves
   const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t w = w4[i];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      // bf16 bit pattern 0x43<nibble> is exactly 128 + nibble
-      const uint32_t pr = ((w >> (4 * m)) & 0x000F000Fu) | 0x43004300u;
-      __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&pr);
-      v = __hmul2(__hsub2(v, off), s2);  // (128 + n - 136) = q exactly, then one rounding of q*s
-      out16[4 * i + m] = *reinterpret_cast<const uint32_t*>(&v);
+      uint32_t pr, q;
+      asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(pr) : "r"(w4[i] >> (4 * m)), "r"(0x000F000Fu), "r"(0x43004300u));
+      asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(pr), "r"(0x43084308u));   // 0x4308 = bf16 136
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(q), "r"(s2));
     }
   }
 }
@@ -491,7 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               uint32_t dq[16];
               dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dq);
               if (ASRC == A_TMEM_DQ) {
-                tmem_st16(lane_base + b * 128 + c * 16, dq);
+                tmem_st8(lane_base + b * 128 + c * 16, dq);
+                tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
               } else {
                 uint8_t* ab = abuf + b * C::kABuf + (c >> 1) * (BM * 128) + l * 128;
 #pragma unroll
