@@ -222,6 +222,22 @@ def dist_setup(n_gpus):
     return ws, rank, local
 
 
+def max_over_ranks(v: float, device=None) -> float:
+    """The largest v over all ranks (v itself with one process). Every rank must call it."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank: int, world: int, seconds_max: float) -> float:
+    """Throughput of the whole job: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / seconds_max
+
+
 def run_reference(args):
     """The oracle as the reference arm: one step = one (token, expert) pair of the workload."""
     ws, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
@@ -337,15 +353,11 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    ms_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     st = layer.check_status()
     if st != 0:
         raise RuntimeError(f"device status after the timed region: {B.moe_status_string(st)}")
-    value = T * world / (ms_max * 1e-3)
+    value = whole_job_tokens_per_s(T, world, ms_max * 1e-3)
 
     # per-kernel pass: the same kernels through the split entry points, events between them
     ksteps = max(10, min(args.steps, 100))
@@ -406,12 +418,8 @@ def run_ours(args):
     for _ in range(esteps):
         layer.forward_host(xh, lh, oh, flags=flags)
         torch.cuda.current_stream(dev).synchronize()
-    e2e_s = (time.perf_counter() - t0) / esteps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": T * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": x.nbytes + logits.nbytes,
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / esteps, dev)
+    e2e = {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": x.nbytes + logits.nbytes,
            "d2h_bytes_per_step": T * s.H * 2, "ms_per_step": e2e_s * 1e3,
            "note": "moe_forward_host: pinned host x/logits -> device, layer, result -> pinned host, stream "
                    "synchronised every step"}

@@ -1,0 +1,54 @@
+"""The multi-rank parts of bench.py on CPU, with two gloo ranks: the slowest
+rank's time is what every rank reports, whole-job throughput counts every
+rank's tokens, and the reference arm runs on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, times, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        ms_max = bench.max_over_ranks(times[rank])
+        out[rank] = (ms_max, bench.whole_job_tokens_per_s(64, world, ms_max * 1e-3))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_report_the_slowest_time_and_all_tokens():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        times = [1.5, 2.5]
+        mp.start_processes(_rank_main, args=(2, _free_port(), times, out), nprocs=2, start_method="spawn")
+        got = dict(out)
+    assert got[0][0] == got[1][0] == 2.5
+    assert got[0][1] == got[1][1] == pytest.approx(2 * 64 / 2.5e-3)
+
+
+def test_single_process_is_its_own_max():
+    import bench
+    assert bench.max_over_ranks(3.25) == 3.25
+    assert bench.whole_job_tokens_per_s(64, 1, 2e-3) == pytest.approx(32000.0)
+
+
+def test_reference_arm_prints_nothing_off_rank_0(monkeypatch, capsys):
+    import argparse
+
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.run_reference(argparse.Namespace(workload="tiny", steps=2, warmup=1, gpus=2))
+    assert capsys.readouterr().out == ""
