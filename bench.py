@@ -48,6 +48,9 @@ WORKLOADS = {
     "decode_t32_shared": dict(shape=synth.FULL_WITH_SHARED, T=32, skew=None),
     "decode_t128_shared": dict(shape=synth.FULL_WITH_SHARED, T=128, skew=None),
     "decode_t512_shared": dict(shape=synth.FULL_WITH_SHARED, T=512, skew=None),
+    # 12 full-size layers (114 GB of int4 + scales) chained as x <- x + MoE_l(RMSNorm(x)); layer l's weights
+    # and router logits use seed l, x seed 0
+    "stack12_t256": dict(shape=synth.FULL, T=256, skew=None, layers=12),
 }
 
 
@@ -70,6 +73,10 @@ def workload_desc(name, w):
     s = w["shape"]
     txt = (f"{name}: routed MoE layer E={s.E} top-{s.top_k} H={s.H} I={s.I}, int4 group-32 weights + bf16 "
            f"scales, bf16 activations, T={w['T']} tokens")
+    if w.get("layers", 1) > 1:
+        txt = (f"{name}: {w['layers']} routed MoE layers E={s.E} top-{s.top_k} H={s.H} I={s.I} chained as "
+               f"x <- x + MoE_l(RMSNorm(x)), int4 group-32 weights + bf16 scales, bf16 activations, "
+               f"T={w['T']} tokens, independent seeded router logits per layer")
     if s.shared_I:
         txt += f", + bf16 shared expert I={s.shared_I}"
     if w["skew"]:
@@ -184,6 +191,24 @@ def _oracle_tokens_per_s(w, budget_s: float, seed=0):
     return len(done) / el, done, el
 
 
+def _oracle_stack_tokens_per_s(w, budget_s: float):
+    """Tokens through layer 0 of the stack (the layers are alike in cost), scaled to all layers."""
+    import oracle
+    s = w["shape"]
+    arrays = synth.make_layer(s, seed=0)
+    x, logits = synth.make_tokens(w["T"], s.H, s.E, seed=0)
+    order = np.random.default_rng(0).permutation(w["T"])
+    done = []
+    t0 = time.perf_counter()
+    for t in order:
+        oracle.stack_layer(x, logits, arrays, s.top_k, tokens=[int(t)])
+        done.append(int(t))
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return len(done) / el / w["layers"], done, el
+
+
 def cpu_baseline(workload: str, budget_s: float = 12.0):
     """Run the oracle in a fresh interpreter with its BLAS threads pinned to the host's core count."""
     cores = os.cpu_count() or 1
@@ -191,14 +216,22 @@ def cpu_baseline(workload: str, budget_s: float = 12.0):
     for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(cores)
     env["CUDA_VISIBLE_DEVICES"] = ""
+    fn = "_oracle_stack_tokens_per_s" if WORKLOADS[workload].get("layers", 1) > 1 else "_oracle_tokens_per_s"
     code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
-            f"v, done, el = bench._oracle_tokens_per_s(bench.WORKLOADS[{workload!r}], {budget_s}); "
+            f"v, done, el = bench.{fn}(bench.WORKLOADS[{workload!r}], {budget_s}); "
             f"print(json.dumps({{'v': v, 'done': done, 'el': el}}))")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                 "sample": f"failed: {r.stderr.strip()[-300:]}"}
     res = json.loads(r.stdout.strip().splitlines()[-1])
+    if WORKLOADS[workload].get("layers", 1) > 1:
+        L = WORKLOADS[workload]["layers"]
+        return {"value": res["v"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": (f"{len(res['done'])} of the {WORKLOADS[workload]['T']} tokens of {workload} through "
+                           f"layer 0 (RMSNorm + routing + 8 experts in fp32 + combine + residual), "
+                           f"{res['el']:.1f} s of CPU work, divided by the {L} layers; numpy/BLAS threads = "
+                           f"{cores}")}
     return {"value": res["v"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": (f"{len(res['done'])} of the {WORKLOADS[workload]['T']} tokens of {workload} "
                        f"(seeded order), each a full layer output (routing + {WORKLOADS[workload]['shape'].top_k} "
@@ -263,7 +296,7 @@ def run_reference(args):
     for i in range(args.steps):
         step(args.warmup + i)
     el = time.perf_counter() - t0
-    value = (args.steps / s.top_k) / el
+    value = (args.steps / s.top_k / w.get("layers", 1)) / el
     cores = os.cpu_count() or 1
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
@@ -272,8 +305,9 @@ def run_reference(args):
         "config": {"workload": workload_desc(args.workload, w), "T": w["T"], "E": s.E, "top_k": s.top_k,
                    "H": s.H, "I": s.I},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"one (token, expert) pair per step, {args.steps} pairs = "
-                                   f"{args.steps / s.top_k:.2f} tokens of {args.workload}; BLAS threads default"},
+                         "sample": f"one (token, expert) pair of layer 0 per step, {args.steps} pairs = "
+                                   f"{args.steps / s.top_k:.2f} token-layers of {args.workload} "
+                                   f"({w.get('layers', 1)} layer(s) per token); BLAS threads default"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -444,6 +478,183 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+def run_stack(args):
+    """A stack of layers: one step = one moe_stack_forward over every layer."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer, MoeW4A16Stack
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    s = w["shape"]
+    T, L, k = w["T"], w["layers"], s.top_k
+    layers, logits_h = [], []
+    for l in range(L):   # one layer's host arrays at a time
+        layers.append(MoeW4A16Layer.from_arrays(s, synth.make_layer(s, seed=l), device=dev))
+        logits_h.append(synth.make_tokens(T, s.H, s.E, seed=l)[1])
+    x, _ = synth.make_tokens(T, s.H, s.E, seed=0)
+    stack = MoeW4A16Stack(layers)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    ld = [torch.from_numpy(v).to(dev) for v in logits_h]
+    out = torch.empty((T, s.H), dtype=torch.int16, device=dev)
+    flags = args.flags
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        stack.forward(xd, ld, out=out, flags=flags)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if stack.check_status() != 0:
+        raise RuntimeError("device status after warm-up: " + B.moe_status_string(stack.check_status()))
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    n0 = B.moe_launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = B.moe_launch_count() - n0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, dev)
+    if stack.check_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    value = whole_job_tokens_per_s(T, world, ms_max * 1e-3)
+
+    # per-kernel pass: every layer through the split entry points, events between the kernels
+    R = T * k
+    d_ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    d_w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    d_off = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
+    d_srt = torch.empty(R, dtype=torch.int32, device=dev)
+    d_inv = torch.empty(R, dtype=torch.int32, device=dev)
+    xn = torch.empty((T, s.H), dtype=torch.int16, device=dev)
+    xperm = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    h = torch.empty((R, s.I), dtype=torch.int16, device=dev)
+    y = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    xa = xd.clone()
+    xb = torch.empty_like(xa)
+    wsp = layers[0].workspace(T)
+    order = 0 if (flags & B.MOE_FLAG_GEMM_SIMT) else B.MOE_FLAG_ROWS_MMA_ORDER
+    names = ["rmsnorm", "route", "permute_gather", "gemm_gate_up", "gemm_down", "combine"]
+    reps = 3
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(L)]
+          for _ in range(reps)]
+    touched = []
+    for r in range(reps):
+        cur, nxt = xa, xb
+        cur.copy_(xd)
+        for l, lay in enumerate(layers):
+            E_ = ev[r][l]
+            E_[0].record(stream)
+            B.moe_rmsnorm(cur, T, s.H, stack.eps, xn)
+            E_[1].record(stream)
+            B.moe_route(ld[l], T, s.E, k, d_ids, d_w)
+            E_[2].record(stream)
+            B.moe_permute(d_ids, T, s.E, k, d_off, d_srt, d_inv, xn, s.H, xperm, wsp, order)
+            E_[3].record(stream)
+            B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, lay.dims, lay.weights, xperm, T, d_off, h, wsp,
+                                     flags | order)
+            E_[4].record(stream)
+            B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, lay.dims, lay.weights, h, T, d_off, y, wsp, flags | order)
+            E_[5].record(stream)
+            B.moe_combine(y, d_inv, d_w, T, k, s.H, cur, nxt)   # the residual as the combine's addend
+            E_[6].record(stream)
+            if r == 0:
+                torch.cuda.synchronize(dev)
+                touched.append(int((np.diff(d_off.cpu().numpy()) > 0).sum()))
+            cur, nxt = nxt, cur
+    torch.cuda.synchronize(dev)
+    per = {n: statistics.mean(ev[r][l][j].elapsed_time(ev[r][l][j + 1]) for r in range(1, reps) for l in range(L))
+           for j, n in enumerate(names)}
+    gu_b, dn_b = expert_bytes(s)
+    alg = {"gemm_gate_up": statistics.mean(t * gu_b for t in touched) + R * s.H * 2 + R * s.I * 2,
+           "gemm_down": statistics.mean(t * dn_b for t in touched) + R * s.I * 2 + R * s.H * 2}
+    dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: per[n])
+    hbm, bf16_burst, bf16_sus, src = load_peaks()
+    achieved = alg[dominant] / (per[dominant] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": profile_traffic(dominant, args.workload), "kernel": dominant, "kernel_ms": per[dominant],
+                "algorithmic_bytes_per_launch": alg[dominant], "peak_source": f"{src} hbm_gbs",
+                "launches_averaged": L * (reps - 1)}
+    step_bytes = sum(t * (gu_b + dn_b) for t in touched) + T * s.H * 2 * 2 + L * T * s.E * 4
+    step_flops = 6.0 * L * T * k * s.H * s.I
+    t_hbm = step_bytes / (hbm * 1e9)
+    t_tc = step_flops / (bf16_sus * 1e12)
+    step_roof = {"touched_experts_per_layer": touched, "bytes": step_bytes, "flops": step_flops,
+                 "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9, "tflops": step_flops / (ms * 1e-3) / 1e12,
+                 "roofline_ms": max(t_hbm, t_tc) * 1e3, "frac": max(t_hbm, t_tc) / (ms * 1e-3),
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "kernels_ms_per_layer": per}
+
+    # end to end: pinned host x and the layers' logits in, host result out, copies inside the timed region
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    lh = [torch.from_numpy(v).pin_memory() for v in logits_h]
+    oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
+    xe = torch.empty_like(xd)
+    le = [torch.empty_like(v) for v in ld]
+
+    def e2e_step():
+        xe.copy_(xh, non_blocking=True)
+        for dst, src_ in zip(le, lh):
+            dst.copy_(src_, non_blocking=True)
+        stack.forward(xe, le, out=out, flags=flags)
+        oh.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    esteps = max(3, min(args.steps, 20))
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(esteps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / esteps, dev)
+    e2e = {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": x.nbytes + sum(v.nbytes for v in logits_h), "d2h_bytes_per_step": T * s.H * 2,
+           "ms_per_step": e2e_s * 1e3,
+           "note": "pinned host x and per-layer logits -> device (torch copies on the stream), moe_stack_forward, "
+                   "result -> pinned host, stream synchronised every step"}
+    if rank != 0:
+        return
+    cpu = cpu_baseline(args.workload) if (world == 1 and not args.no_cpu_baseline) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, w), "T": T, "layers": L, "E": s.E, "top_k": k,
+                   "H": s.H, "I": s.I, "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: each step streams {sum(touched) * (gu_b + dn_b) / 1e9:.1f} GB of int4 weights "
+                         f"through a 129 MB L2", "flags": flags},
+        "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,6 +669,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif WORKLOADS[args.workload].get("layers", 1) > 1:
+        run_stack(args)
     else:
         run_ours(args)
 

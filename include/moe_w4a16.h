@@ -239,6 +239,30 @@ MOE_API moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, cons
                               const float* logits_host, int32_t T, uint16_t* out_host,
                               void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* Parameter-free RMSNorm of each row: out[t][i] = bf16(x[t][i] / r_t) with
+ * r_t = sqrt(mean_i x[t][i]^2 + eps), in fp32 (squares summed, one IEEE
+ * square root, one IEEE division per element). x, out bf16 [T][H], H a
+ * multiple of 8; out may not overlap x. */
+MOE_API moe_status_t moe_rmsnorm(const uint16_t* x, int32_t T, int32_t H, float eps, uint16_t* out, void* stream);
+
+/* A stack of L routed-expert layers joined as pre-norm residual blocks,
+ *   x_{l+1} = x_l + MoE_l(RMSNorm(x_l)),   l = 0 .. L-1,   out = x_L.
+ * The catalog page gives 60 MoE layers of this shape ("Kimi-K2.6", GEOMETRY)
+ * but not how they are joined; a bare x + MoE(x) grows without bound within
+ * a few layers, and the usual pre-norm residual with a parameter-free norm is
+ * the reading used here. Each layer's residual add happens inside its combine
+ * (fp32, one bf16 rounding together with the layer's output).
+ *   layers: HOST array of L weight sets (all with the same shared_I);
+ *   logits: HOST array of L DEVICE pointers, fp32 [T][E] each (the router
+ *           logits of each layer are inputs here);
+ *   x, out: bf16 [T][H]; out may equal x.
+ * ws_bytes >= moe_stack_workspace_size(d, T, shared_I, flags). The status word
+ * is the workspace's, as for moe_forward. */
+MOE_API size_t moe_stack_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags);
+MOE_API moe_status_t moe_stack_forward(moe_dims_t d, const moe_weights_t* layers, int32_t L,
+                               const float* const* logits, const uint16_t* x, int32_t T, float eps,
+                               uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
 /* Synchronises `stream`, reads the workspace status word, resets it to 0 and
  * returns it (MOE_OK if no device error was recorded since the last check). */
 MOE_API moe_status_t moe_check_status(void* ws, void* stream);

@@ -41,7 +41,7 @@ __all__ = [
     "bf16_to_f32", "exp_def", "sigmoid_def", "route", "permute",
     "unpack_int4", "pack_int4", "dequant", "silu", "expert_mlp",
     "shared_expert", "combine", "moe_layer", "gateup_rows", "down_rows",
-    "rmsnorm", "expert_int4_params", "EXP_CONSTANTS",
+    "rmsnorm", "stack_layer", "f32_to_bf16", "expert_int4_params", "EXP_CONSTANTS",
 ]
 
 
@@ -52,6 +52,19 @@ __all__ = [
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns (uint16) -> fp32 values (exact: bf16 is the top half of fp32)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f32_to_bf16(v: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns, rounded to nearest with ties to even (NaN stays NaN).
+
+    Keep the top 16 bits after adding 0x7FFF plus the lowest kept bit: below
+    half an ulp rounds down, above rounds up, an exact half rounds to the even
+    neighbour.
+    """
+    u = np.asarray(v, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(np.asarray(v, dtype=np.float32))
+    return np.where(nan, np.uint16(0x7FC0), r).astype(np.uint16)
 
 
 # ---------------------------------------------------------------------------
@@ -304,3 +317,20 @@ def rmsnorm(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     x = np.asarray(x, dtype=np.float32)
     ms = np.mean(x.astype(np.float32) * x, axis=-1, keepdims=True, dtype=np.float32)
     return (x / np.sqrt(ms + F32(eps))).astype(np.float32)
+
+
+def stack_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, eps: float = 1e-6, tokens=None,
+                with_shared: bool = False) -> dict:
+    """One block of the layer stack, x + MoE(RMSNorm(x)), for ``tokens`` (all by default).
+
+    The pages give 60 MoE layers ("Kimi-K2.6", GEOMETRY) but not how they are
+    joined; the reading used is the pre-norm residual with a parameter-free
+    RMSNorm. The normalised activations enter the layer as bf16 (the layer's
+    input type), the residual add is fp32. Returns moe_layer's dict with
+    ``out`` = x + MoE(...) in fp32.
+    """
+    xn_bits = f32_to_bf16(rmsnorm(bf16_to_f32(x_bits), eps))
+    res = moe_layer(xn_bits, logits, layer, k, tokens=tokens, with_shared=with_shared)
+    res["out"] = (bf16_to_f32(x_bits[res["tokens"]]) + res["out"]).astype(np.float32)
+    res["xn_bits"] = xn_bits
+    return res

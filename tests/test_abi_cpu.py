@@ -96,4 +96,18 @@ def test_arguments_rejected_before_any_launch(lib):
     assert L.moe_check_status(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_debug_expire_wait(None, 1000, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward_host(d, byref(w), None, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_rmsnorm(None, 4, 256, 1e-6, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_rmsnorm(16, 4, 250, 1e-6, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_rmsnorm(16, 4, 256, -1.0, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_rmsnorm(16, 0, 256, 1e-6, 16, None) == B.MOE_OK                # T == 0: no-op
+    two = (B.moe_weights_t * 2)(w, w)
+    lg = (ctypes.c_void_p * 2)(16, 16)
+    assert L.moe_stack_forward(d, two, 0, lg, 16, 4, 1e-6, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    mixed = (B.moe_weights_t * 2)(w, B.moe_weights_t(16, 16, 16, 16, 16, 16, 64))   # shared_I differs
+    assert L.moe_stack_forward(d, mixed, 2, lg, 16, 4, 1e-6, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_forward(d, two, 2, (ctypes.c_void_p * 2)(16, None), 16, 4, 1e-6, 16, 16, 1 << 30, 0,
+                               None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_stack_forward(d, two, 2, lg, 16, 4, 1e-6, 16, 16, 4096, 0, None) == \
+        B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_stack_workspace_size(d, 4, 0, 0) == L.moe_workspace_size(d, 4, 0, 0) + 3 * 2048
     assert L.moe_launch_count() == 0                                           # nothing launched

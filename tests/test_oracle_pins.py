@@ -345,3 +345,66 @@ def test_rmsnorm_unit_rms():
     x = np.random.default_rng(0).standard_normal((4, 256)).astype(np.float32) * 7
     n = oracle.rmsnorm(x)
     assert np.abs(np.sqrt(np.mean(n.astype(np.float64) ** 2, axis=1)) - 1).max() < 1e-5
+
+
+# ---------------------------------------------------------------------------
+# bf16 rounding and the layer stack
+# ---------------------------------------------------------------------------
+
+def nearest_bf16_bits(v: float) -> int:
+    """Brute force: of the bf16 values bracketing v, the nearer; on a tie the one with an even pattern."""
+    from fractions import Fraction
+    u = struct.unpack(">I", struct.pack(">f", v))[0]
+    lo = u >> 16
+    cands = [lo, lo + 1]
+    fv = Fraction(v)
+    best = min(cands, key=lambda b: (abs(Fraction(bf16_bits_to_float(b)) - fv), b & 1))
+    return best
+
+
+def test_f32_to_bf16_rounds_to_nearest_even():
+    one = 1.0
+    cases = [one, one + 2.0 ** -8, one + 3 * 2.0 ** -8, one + 2.0 ** -8 + 2.0 ** -20, -(one + 2.0 ** -8),
+             -(one + 3 * 2.0 ** -8), 3.0e38, 1e-40, 0.0, -0.0, 65504.0, 7.0]
+    got = oracle.f32_to_bf16(np.array(cases, dtype=np.float32))
+    assert got[0] == 0x3F80
+    assert got[1] == 0x3F80            # tie -> even (down)
+    assert got[2] == 0x3F82            # tie -> even (up)
+    assert got[3] == 0x3F81            # just above the tie -> up
+    assert got[4] == 0xBF80 and got[5] == 0xBF82
+    assert got[8] == 0x0000 and got[9] == 0x8000
+    vals = np.random.default_rng(3).standard_normal(2000).astype(np.float32) * np.float32(37.0)
+    got = oracle.f32_to_bf16(vals)
+    for v, g in zip(vals, got):
+        assert int(g) == nearest_bf16_bits(float(v))
+    assert oracle.f32_to_bf16(np.array([np.nan], dtype=np.float32))[0] & 0x7F80 == 0x7F80
+
+
+def test_stack_layer_with_zero_weights_is_the_identity():
+    import synth
+    E, H, I = 3, 64, 32
+    layer = rand_layer(E, H, I, seed=6)
+    layer["w13"][:] = np.int32(np.uint32(0x88888888).view(np.int32))
+    layer["w2"][:] = np.int32(np.uint32(0x88888888).view(np.int32))
+    x_bits, logits = synth.make_tokens(5, H, E, seed=3)
+    res = oracle.stack_layer(x_bits, logits, layer, k=2)
+    assert np.array_equal(res["out"], oracle.bf16_to_f32(x_bits))
+
+
+def test_stack_layer_single_expert_equals_brute_force():
+    """E=1, top-1: x + MLP(bf16(x / sqrt(mean(x^2) + eps))), written out in fp64 loops."""
+    import synth
+    H, I, eps = 64, 32, 1e-6
+    layer = rand_layer(1, H, I, seed=21)
+    x_bits, logits = synth.make_tokens(3, H, 1, seed=5)
+    res = oracle.stack_layer(x_bits, logits, layer, k=1, eps=eps)
+    for t in range(3):
+        x = [bf16_bits_to_float(b) for b in x_bits[t]]
+        r = math.sqrt(sum(v * v for v in x) / H + eps)
+        xn = [bf16_bits_to_float(nearest_bf16_bits(v / r)) for v in x]
+        mlp = brute_expert(xn, layer["w13"][0], layer["s13"][0], layer["w2"][0], layer["s2"][0])
+        ref = np.array([a + b for a, b in zip(x, mlp)])
+        got = res["out"][t].astype(np.float64)
+        # fp32 against fp64 normalisation may put a few inputs one bf16 step apart
+        assert np.abs(got - ref).max() <= 1e-2 * np.sqrt(np.mean(np.array(mlp) ** 2)) + 1e-6
+        assert np.abs(got - ref).mean() <= 1e-4 * np.sqrt(np.mean(np.array(mlp) ** 2)) + 1e-6

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, Structure, c_char_p, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
+from ctypes import c_float, POINTER, Structure, c_char_p, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_w4a16.so")
 
@@ -67,6 +67,10 @@ SIGNATURES = {
     "moe_host_staging_size": (c_size_t, [moe_dims_t, c_int32]),
     "moe_forward_host": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_void_p, c_int32,
                                    c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_rmsnorm": (c_int32, [c_void_p, c_int32, c_int32, c_float, c_void_p, c_void_p]),
+    "moe_stack_workspace_size": (c_size_t, [moe_dims_t, c_int32, c_int32, c_uint32]),
+    "moe_stack_forward": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_int32, POINTER(c_void_p), c_void_p,
+                                    c_int32, c_float, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_check_status": (c_int32, [c_void_p, c_void_p]),
     "moe_launch_count": (c_uint64, []),
     "moe_debug_expire_wait": (c_int32, [c_void_p, c_int64, c_void_p]),
@@ -214,6 +218,26 @@ def moe_forward_host(d: moe_dims_t, w: moe_weights_t, x_host, logits_host, T: in
             raise ValueError("moe_forward_host takes host tensors")
     _check(load().moe_forward_host(d, ctypes.byref(w), _ptr(x_host), _ptr(logits_host), T, _ptr(out_host),
                                    _dptr(ws), _nbytes(ws), flags, _stream(stream)), "moe_forward_host")
+
+
+def moe_rmsnorm(x, T: int, H: int, eps: float, out, stream=None) -> None:
+    _check(load().moe_rmsnorm(_dptr(x), T, H, eps, _dptr(out), _stream(stream)), "moe_rmsnorm")
+
+
+def moe_stack_workspace_size(d: moe_dims_t, T: int, shared_I: int = 0, flags: int = 0) -> int:
+    return int(load().moe_stack_workspace_size(d, T, shared_I, flags))
+
+
+def moe_stack_forward(d: moe_dims_t, layers, logits, x, T: int, eps: float, out, ws, flags: int = 0,
+                      stream=None) -> None:
+    """layers: list of moe_weights_t; logits: list of device tensors fp32 [T][E], one per layer."""
+    L = len(layers)
+    if len(logits) != L:
+        raise ValueError("one logits tensor per layer")
+    arr = (moe_weights_t * L)(*layers)
+    lp = (c_void_p * L)(*[_dptr(t) for t in logits])
+    _check(load().moe_stack_forward(d, arr, L, lp, _dptr(x), T, eps, _dptr(out), _dptr(ws), _nbytes(ws), flags,
+                                    _stream(stream)), "moe_stack_forward")
 
 
 def moe_check_status(ws, stream=None) -> int:

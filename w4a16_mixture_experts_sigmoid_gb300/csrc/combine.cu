@@ -1,6 +1,7 @@
 // Step 5: the top-k weighted combine back to token order,
-//   out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]]  (+ addend[t]) ),
-// fp32 accumulation in rank order j, one rounding to bf16 at the end.
+//   out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]]  (+ addend[t])  (+ residual[t]) ),
+// fp32 accumulation in rank order j, then the shared expert's output, then the
+// residual stream of a layer stack, one rounding to bf16 at the end.
 // The pages' MoE sums the selected experts' outputs per token ("feat(pytorch):
 // support Kimi K2.6", MoE routing); where the weights enter is not spelled out,
 // and multiplying after the down projection is the reading used here.
@@ -27,7 +28,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // grid: (ceil(H/8 / blockDim), T); each thread owns 8 consecutive columns of one token.
 __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k, int H8,
-                                                      const uint4* __restrict__ addend, uint4* __restrict__ out) {
+                                                      const uint4* __restrict__ addend,
+                                                      const uint4* __restrict__ residual, uint4* __restrict__ out) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H8) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
@@ -49,6 +51,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] += f[i];
   }
+  if (residual != nullptr) {
+    float f[8];
+    unpack8(__ldg(residual + (int64_t)t * H8 + c), f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += f[i];
+  }
   uint4 o;
   o.x = pack_bf16x2(acc[0], acc[1]);
   o.y = pack_bf16x2(acc[2], acc[3]);
@@ -61,12 +69,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
-                           const uint16_t* addend, uint16_t* out, cudaStream_t s) {
+                           const uint16_t* addend, const uint16_t* residual, uint16_t* out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int H8 = H / 8;
   dim3 grid((H8 + 127) / 128, T < 65535 ? T : 65535);
   combine_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const uint4*>(y), inv, w, T, k, H8,
-                                      reinterpret_cast<const uint4*>(addend), reinterpret_cast<uint4*>(out));
+                                      reinterpret_cast<const uint4*>(addend), reinterpret_cast<const uint4*>(residual),
+                                      reinterpret_cast<uint4*>(out));
   count_launches(1);
   return cudaGetLastError();
 }

@@ -28,7 +28,9 @@ cudaError_t launch_to_mma_order(const uint16_t* src, uint16_t* dst, int64_t rows
 
 // combine
 cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
-                           const uint16_t* addend, uint16_t* out, cudaStream_t s);
+                           const uint16_t* addend, const uint16_t* residual, uint16_t* out, cudaStream_t s);
+// out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), fp32 arithmetic
+cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out, cudaStream_t s);
 
 // grouped GEMM problem description shared by both GEMM implementations
 struct GemmProblem {

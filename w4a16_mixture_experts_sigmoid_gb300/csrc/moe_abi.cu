@@ -205,8 +205,10 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   return MOE_OK;
 }
 
+// One layer. residual (nullable, [T][H]) is added to the output in the combine's fp32 sum.
 moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, const float* logits,
-                            int32_t T, uint16_t* out, uint8_t* ws, uint32_t flags, int sms, cudaStream_t s) {
+                            int32_t T, const uint16_t* residual, uint16_t* out, uint8_t* ws, uint32_t flags, int sms,
+                            cudaStream_t s) {
   const Layout L = layout(d, T, w->shared_I);
   int* status = reinterpret_cast<int*>(ws);
   int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
@@ -238,7 +240,7 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
     if (st != MOE_OK) return st;
     addend = ys;
   }
-  return cuda_status(launch_combine(y, inv, tw, T, d.top_k, d.H, addend, out, s));
+  return cuda_status(launch_combine(y, inv, tw, T, d.top_k, d.H, addend, residual, out, s));
 }
 
 }  // namespace
@@ -375,7 +377,7 @@ moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const 
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
-  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, out, as_stream(stream)));
+  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, nullptr, out, as_stream(stream)));
 }
 
 moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits, int32_t T,
@@ -390,7 +392,8 @@ moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x
   if (ws_bytes < layout(d, T, w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
-  return forward_device(d, w, x, logits, T, out, static_cast<uint8_t*>(ws), flags, di.sms, as_stream(stream));
+  return forward_device(d, w, x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
+                        as_stream(stream));
 }
 
 moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host, const float* logits_host,
@@ -415,7 +418,7 @@ moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16
   cudaStream_t s = as_stream(stream);
   if (cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpyAsync(dl, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = forward_device(d, w, dx, dl, T, dout, w8, flags, di.sms, s);
+  st = forward_device(d, w, dx, dl, T, nullptr, dout, w8, flags, di.sms, s);
   if (st != MOE_OK) return st;
   return cuda_status(cudaMemcpyAsync(out_host, dout, xb, cudaMemcpyDeviceToHost, s));
 }
@@ -427,6 +430,60 @@ moe_status_t moe_check_status(void* ws, void* stream) {
   if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   return static_cast<moe_status_t>(v);
+}
+
+moe_status_t moe_rmsnorm(const uint16_t* x, int32_t T, int32_t H, float eps, uint16_t* out, void* stream) {
+  if (T < 0 || H < 8 || H % 8 || H > kMaxDim || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || out == nullptr || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_rmsnorm(x, T, H, eps, out, as_stream(stream)));
+}
+
+size_t moe_stack_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags) {
+  const size_t base = moe_workspace_size(d, T, shared_I, flags);
+  if (base == 0) return 0;
+  return base + 3 * align256(static_cast<size_t>(T) * d.H * 2);
+}
+
+moe_status_t moe_stack_forward(moe_dims_t d, const moe_weights_t* layers, int32_t L, const float* const* logits,
+                               const uint16_t* x, int32_t T, float eps, uint16_t* out, void* ws, size_t ws_bytes,
+                               uint32_t flags, void* stream) {
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if (L < 1 || layers == nullptr || logits == nullptr || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  int32_t shared_I = 0;
+  for (int32_t l = 0; l < L; ++l) {
+    if ((st = check_weights(&layers[l], false)) != MOE_OK) return st;
+    if (l > 0 && layers[l].shared_I != shared_I) return MOE_ERR_INVALID_ARG;   // one workspace layout for all
+    shared_I = layers[l].shared_I;
+  }
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || out == nullptr || ws == nullptr || !aligned16(x) || !aligned16(out) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  for (int32_t l = 0; l < L; ++l)
+    if (logits[l] == nullptr) return MOE_ERR_INVALID_ARG;
+  const size_t base = layout(d, T, shared_I).end;
+  const size_t xb = align256(static_cast<size_t>(T) * d.H * 2);
+  if (ws_bytes < base + 3 * xb) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + base);
+  uint16_t* ping[2] = {reinterpret_cast<uint16_t*>(w8 + base + xb), reinterpret_cast<uint16_t*>(w8 + base + 2 * xb)};
+  cudaStream_t s = as_stream(stream);
+  const uint16_t* cur = x;
+  for (int32_t l = 0; l < L; ++l) {
+    uint16_t* next = (l == L - 1) ? out : ping[l & 1];
+    if (launch_rmsnorm(cur, T, d.H, eps, xn, s) != cudaSuccess) return MOE_ERR_CUDA;
+    st = forward_device(d, &layers[l], xn, logits[l], T, cur, next, w8, flags, di.sms, s);
+    if (st != MOE_OK) return st;
+    cur = next;
+  }
+  return MOE_OK;
 }
 
 uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }

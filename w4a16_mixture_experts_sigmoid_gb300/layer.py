@@ -75,3 +75,43 @@ class MoeW4A16Layer:
 
     def check_status(self, stream=None) -> int:
         return 0 if self._ws is None else B.moe_check_status(self._ws, stream)
+
+
+class MoeW4A16Stack:
+    """Layers chained as pre-norm residual blocks, x <- x + MoE_l(RMSNorm(x)), in one C call
+    (moe_stack_forward). Every layer's weights stay resident; the router logits of each layer
+    are inputs."""
+
+    def __init__(self, layers: list, eps: float = 1e-6):
+        if not layers:
+            raise ValueError("a stack needs at least one layer")
+        first = layers[0]
+        for lay in layers:
+            if (lay.E, lay.top_k, lay.H, lay.I, lay.shared_I) != (first.E, first.top_k, first.H, first.I,
+                                                                   first.shared_I):
+                raise ValueError("all layers of a stack must have the same shape")
+        self.layers = layers
+        self.eps = float(eps)
+        self.dims = first.dims
+        self.H = first.H
+        self.shared_I = first.shared_I
+        self.device = first.device
+        self._ws = None
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = B.moe_stack_workspace_size(self.dims, T, self.shared_I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, logits: list, out: torch.Tensor | None = None, flags: int = 0,
+                stream=None) -> torch.Tensor:
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.int16, device=self.device)
+        B.moe_stack_forward(self.dims, [lay.weights for lay in self.layers], logits, x, T, self.eps, out,
+                            self.workspace(T), flags, stream)
+        return out
+
+    def check_status(self, stream=None) -> int:
+        return 0 if self._ws is None else B.moe_check_status(self._ws, stream)
