@@ -43,6 +43,9 @@ WORKLOADS = {
     # profiling-sized decode: 48 full-size experts (1.2 GB of int4 + scales, ~9x L2), T=8 -> 1.33 rows per
     # expert as in decode_t64; used for ncu captures that must stay a few GB on the device
     "decode_e48_t8": dict(shape=synth.LayerShape(E=48, top_k=8, H=7168, I=2048), T=8, skew=None),
+    # profiling-sized prefill: 48 full-size experts, T=512 -> ~85 rows per expert (128-row token tiles as in
+    # prefill_t4096_zipf, whose mean is 85)
+    "prefill_e48_t512": dict(shape=synth.LayerShape(E=48, top_k=8, H=7168, I=2048), T=512, skew=None),
     "decode_t1_shared": dict(shape=synth.FULL_WITH_SHARED, T=1, skew=None),
     "decode_t8_shared": dict(shape=synth.FULL_WITH_SHARED, T=8, skew=None),
     "decode_t32_shared": dict(shape=synth.FULL_WITH_SHARED, T=32, skew=None),
