@@ -67,6 +67,7 @@ constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BK = 256;            // K per pipeline stage
 constexpr int KSUB = 64;           // K per 128-byte swizzle row
 constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
+constexpr int kThreads = 512;      // 16 warps, 128 registers a thread
 constexpr int kFirstDqWarp = 2;
 constexpr int kFirstEpiWarp = 10;
 constexpr int kBProducerWarp = 14;
@@ -79,7 +80,7 @@ constexpr int kAuxBytes = 7168;
 struct TcParams {
   CUtensorMap tm_w;  // int4 words [rows_total][K/8] (box 32 x 64) or bf16 weights [rows_total][K] (box 64 x 16)
   CUtensorMap tm_s;  // bf16 scales [rows_total][K/32] (box 8 x 64), when scale_tma
-  CUtensorMap tm_b[5];  // bf16 token rows [R][K], box 64 x (8 << i) rows (the boxes up to NT rows are set)
+  CUtensorMap tm_b;  // bf16 token rows [R][K] (box 64 x NT)
   const uint16_t* scales;
   const int32_t* offsets;
   uint16_t* out;
@@ -93,9 +94,6 @@ struct TcParams {
 // the stage in registers, so HBM streaming never waits on the tensor pipe; the
 // token-row ring (operand B) is released by the MMA commit. With dense bf16
 // weights the MMA reads both, and the two rings advance in lock step.
-constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }
-constexpr int lcm_c(int a, int b) { return a / gcd_c(a, b) * b; }
-
 template <int ASRC, int NT>
 struct Cfg {
   static constexpr bool kDq = ASRC != A_SMEM_BF16;
@@ -112,21 +110,15 @@ struct Cfg {
   static constexpr int kLock = kAvail / (kWStage + kBStage);
   static constexpr int kWStages = kDq ? (kWStagesDq > 12 ? 12 : kWStagesDq) : (kLock > 8 ? 8 : kLock);
   static constexpr int kBStages = kDq ? kBStagesDq : kWStages;
-  // MMA issuers, each with its own accumulators. A thread issues an M=128 MMA only every ~70
-  // cycles, and every ~125 while the dequant warps store into tensor memory, but several threads
-  // issue in parallel: up to 64 tokens per tile two issuers, 128 tokens one. (A third issuer in a
-  // 17th warp measured slower on 16-token tiles.)
-  static constexpr int kMmaGroups = NT <= 64 ? 2 : 1;
-  static constexpr int kThreads = 512;   // 16 warps, 128 registers a thread
   // try_wait.parity cannot tell phase k from phase k+2, so a barrier may be waited on only by a
-  // consumer that cannot run two phases ahead of it. Stages alternate between two dequant groups
-  // (g % 2) and between the issuers (g % kMmaGroups), so every "full" barrier and every A-buffer
-  // barrier is kept per (g % kL, slot), kL = lcm(2, kMmaGroups) = 2: the stages that share one are
-  // lcm(kL, ring) apart and are all taken by one dequant group and one issuer, in order.
-  static constexpr int kL = lcm_c(2, kMmaGroups);
-  static constexpr int kWPeriod = lcm_c(kL, kWStages);
-  static constexpr int kBPeriod = lcm_c(kL, kBStages);
-  static constexpr int kAPeriod = lcm_c(kL, kNBuf);
+  // consumer that cannot run two phases ahead of it. Stages alternate between two consumers
+  // (dequant groups, MMA issuers) by g % 2, so every "full" barrier and every A-buffer barrier
+  // is kept per (g % 2, slot): the stages that share one are lcm(2, ring) apart and are all
+  // taken by one consumer in order.
+  static constexpr int kWPeriod = (kWStages % 2 == 0) ? kWStages : 2 * kWStages;
+  static constexpr int kBPeriod = (kBStages % 2 == 0) ? kBStages : 2 * kBStages;
+  static constexpr int kAPeriod = (kNBuf % 2 == 0) ? kNBuf : 2 * kNBuf;
+  static constexpr int kMmaGroups = NT <= 64 ? 2 : 1;   // MMA issuers, each with its own accumulators
   static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
   static constexpr int kColsNeeded = kAccCol + 2 * kMmaGroups * NT;   // double-buffered per issuer
   static constexpr int kTmemCols = kColsNeeded <= 32 ? 32 : kColsNeeded <= 64 ? 64 : kColsNeeded <= 128 ? 128
@@ -135,27 +127,11 @@ struct Cfg {
       kAlignSlack + kWStages * kWStage + kBStages * kBStage + kNBuf * kABuf + kAuxBytes;
   static_assert(kWStages >= 2 && kBStages >= 2, "each ring needs at least two stages");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory overflow");
-  static_assert(8 * ((kL + 1) * (kWStages + kBStages) + 2 * kL * kNBuf + 5) + 16 + 2 * kMaxE + 4 * (kMaxE + 1) <=
-                    kAuxBytes,
+  static_assert(8 * (3 * kWStages + 3 * kBStages + 4 * kNBuf + 5) + 16 + 2 * kMaxE + 4 * (kMaxE + 1) <= kAuxBytes,
                 "barriers and tile table overflow the aux area");
   static_assert(kColsNeeded <= 512, "tensor memory overflow");
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
-
-// Token rows a tile really loads and multiplies: the tile's valid rows rounded up to a power of
-// two, at least 8 rows loaded (box_rows) and at least 16 multiplied (mma_n, the smallest N of an
-// M=128 MMA), at most NT. Rows past the valid ones only feed accumulator columns the epilogue
-// never reads (column n of the product depends on token row n alone).
-__device__ __forceinline__ int box_index(int nvalid, int nt) {
-  int k = 0;
-  while ((8 << k) < nvalid && (8 << k) < nt) ++k;
-  return k;
-}
-__device__ __forceinline__ int mma_n(int nvalid, int nt) {
-  int n = 16;
-  while (n < nvalid && n < nt) n <<= 1;
-  return n;
-}
 
 struct TileInfo {
   int wt;      // weight tile (128 rows; for gate/up 64 gate + 64 up rows)
@@ -229,7 +205,7 @@ __device__ __forceinline__ int a_releases_needed(int g, int nb, int period) {
 __device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1); }
 
 template <int OP, int ASRC, int NT>
-__global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<ASRC, NT>;
   constexpr int SW = C::kWStages;
   constexpr int SB = C::kBStages;
@@ -239,15 +215,13 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
   uint8_t* bring = smem + SW * C::kWStage;
   uint8_t* abuf = bring + SB * C::kBStage;
   uint8_t* aux = abuf + NB * C::kABuf;
-  constexpr int L = C::kL;
-  constexpr int G = C::kMmaGroups;
-  uint64_t* wfull = reinterpret_cast<uint64_t*>(aux);   // [L][SW]: (stage class g % L, slot)
-  uint64_t* wempty = wfull + L * SW;
-  uint64_t* bfull = wempty + SW;                         // [L][SB]
-  uint64_t* bempty = bfull + L * SB;
-  uint64_t* afull = bempty + SB;      // [L][NB]: (stage class, A buffer)
-  uint64_t* aempty = afull + L * NB;  // [L][NB]
-  uint64_t* accfull = aempty + L * NB;   // [2]
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(aux);   // [2][SW]: (stage parity, slot)
+  uint64_t* wempty = wfull + 2 * SW;
+  uint64_t* bfull = wempty + SW;                         // [2][SB]
+  uint64_t* bempty = bfull + 2 * SB;
+  uint64_t* afull = bempty + SB;      // [2][NB]: (dequant group, A buffer)
+  uint64_t* aempty = afull + 2 * NB;  // [2][NB]
+  uint64_t* accfull = aempty + 2 * NB;   // [2]
   uint64_t* accempty = accfull + 2;  // [2]
   uint64_t* drain = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -261,13 +235,13 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
   const int nk = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L * SW; ++s) mbar_init(&wfull[s], 32);
+    for (int s = 0; s < 2 * SW; ++s) mbar_init(&wfull[s], 32);
     for (int s = 0; s < SW; ++s) mbar_init(&wempty[s], C::kDq ? 4 : 1);
-    for (int s = 0; s < L * SB; ++s) mbar_init(&bfull[s], 1);
+    for (int s = 0; s < 2 * SB; ++s) mbar_init(&bfull[s], 1);
     for (int s = 0; s < SB; ++s) mbar_init(&bempty[s], 1);
-    for (int b = 0; b < L * NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], G); mbar_init(&accempty[a], 4); }
-    mbar_init(drain, G);
+    for (int b = 0; b < 2 * NB; ++b) { mbar_init(&afull[b], 4); mbar_init(&aempty[b], 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(&accfull[a], C::kMmaGroups); mbar_init(&accempty[a], 4); }
+    mbar_init(drain, C::kMmaGroups);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -332,7 +306,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
       else { grow_lo = ebase + ti.wt * BM; grow_hi = grow_lo + 64; }
       for (int ks = 0; ks < nk; ++ks, ++g) {
         const int sw = g % SW;
-        uint64_t* wf = &wfull[(g % L) * SW + sw];
+        uint64_t* wf = &wfull[(g & 1) * SW + sw];
         if (!warp_wait(&wempty[sw], ((g / SW) & 1) ^ 1, p, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + sw * C::kWStage;
         uint8_t* ss = sa + C::kAStage;
@@ -381,7 +355,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
     if (lane == 0) {
       for (int d = 0; d < SW && d < g; ++d) {
         const int gg = g - 1 - d;
-        mbar_wait(&wfull[(gg % L) * SW + gg % SW], (gg / C::kWPeriod) & 1, p.timeout_ns, nullptr, p.status);
+        mbar_wait(&wfull[(gg & 1) * SW + gg % SW], (gg / C::kWPeriod) & 1, p.timeout_ns, nullptr, p.status);
       }
     }
     __syncwarp();
@@ -389,59 +363,56 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
     // ------------------------------------------------------------ token-row producer (one lane)
     if (lane == 0) {
       const uint64_t pol_b = l2_policy_evict_last();
+      constexpr uint32_t txb = NSUB * NT * 128;
       int g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
         const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
-        const int bk = box_index(ti.nvalid, NT);
-        const CUtensorMap* tmb = &p.tm_b[bk];
-        const uint32_t txb = NSUB * (8u << bk) * 128u;
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int sbi = g % SB;
           if (!mbar_wait(&bempty[sbi], ((g / SB) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sb = bring + sbi * C::kBStage;
-          uint64_t* bf = &bfull[(g % L) * SB + sbi];
+          uint64_t* bf = &bfull[(g & 1) * SB + sbi];
           mbar_arrive_expect_tx(bf, txb);
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sb + sub * (NT * 128), tmb, bf, ks * BK + sub * KSUB, ti.row0, pol_b);
+            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, bf, ks * BK + sub * KSUB, ti.row0, pol_b);
         }
       }
       for (int d = 0; d < SB && d < g; ++d) {
         const int gg = g - 1 - d;
-        mbar_wait(&bfull[(gg % L) * SB + gg % SB], (gg / C::kBPeriod) & 1, p.timeout_ns, nullptr, p.status);
+        mbar_wait(&bfull[(gg & 1) * SB + gg % SB], (gg / C::kBPeriod) & 1, p.timeout_ns, nullptr, p.status);
       }
     }
     __syncwarp();
-  } else if (warp == 1 || (G == 2 && warp == kSecondMmaWarp)) {
+  } else if (warp == 1 || (C::kMmaGroups == 2 && warp == kSecondMmaWarp)) {
     // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
-      // issuer mg takes the stages g with g % G == mg
-      const int mg = (warp == 1) ? 0 : 1;
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, NT);
+      const int mg = (warp == 1) ? 0 : 1;  // with two issuers, issuer mg takes the stages g with g % 2 == mg
       int g = 0, it = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
-        const uint32_t idesc = idesc_bf16_f32(BM, mma_n(decode_tile(i, n_act, act_e, tpre, p, NT).nvalid, NT));
         const int ab = it & 1;
         if (!mbar_wait(&accempty[ab], ((it >> 1) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol + (mg * 2 + ab) * NT;
         bool first = true;
         for (int ks = 0; ks < nk; ++ks, ++g) {
-          if (G > 1 && g % G != mg) continue;
+          if (C::kMmaGroups == 2 && (g & 1) != mg) continue;
           const int sw = g % SW, sbi = g % SB;
           const int b = g % NB;
-          if (!mbar_wait(&bfull[(g % L) * SB + sbi], (g / C::kBPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+          if (!mbar_wait(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
             ok = false;
             break;
           }
           if (C::kDq) {
-            if (!mbar_wait(&afull[(g % L) * NB + b], (g / C::kAPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+            if (!mbar_wait(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
               ok = false;
               break;
             }
           } else {
-            if (!mbar_wait(&wfull[(g % L) * SW + sw], (g / C::kWPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+            if (!mbar_wait(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
               ok = false;
               break;
             }
@@ -467,7 +438,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
           }
           first = false;
           mma_commit(&bempty[sbi]);
-          if (C::kDq) mma_commit(&aempty[((g + NB) % L) * NB + b]);   // under the class of its next user
+          if (C::kDq) mma_commit(&aempty[((g + NB) & 1) * NB + b]);   // to the group of the next user
           else mma_commit(&wempty[sw]);
         }
         if (!ok) break;
@@ -494,7 +465,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
           const int sw = g % SW;
           const int b = g % NB;
           const int a_need = a_releases_needed(g, NB, C::kAPeriod);
-          if (!warp_wait(&wfull[(g % L) * SW + sw], (g / C::kWPeriod) & 1, p, abort_flag)) { ok = false; break; }
+          if (!warp_wait(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p, abort_flag)) { ok = false; break; }
           // the stage row comes into registers in two halves of four 16-byte chunks; once the
           // second half is loaded the stage goes back to the producer
           const uint8_t* arow = smem + sw * C::kWStage + r_sm * 128;
@@ -503,10 +474,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
           uint4 wv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
-          if (a_need > 0 && !warp_wait(&aempty[(g % L) * NB + b], (a_need - 1) & 1, p, abort_flag)) {
-            ok = false;
-            break;
-          }
+          if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
@@ -538,7 +506,7 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
           else fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[(g % L) * NB + b]);
+          if (lane == 0) mbar_arrive(&afull[grp * NB + b]);
         }
       }
     }
@@ -553,27 +521,25 @@ __global__ void __launch_bounds__(Cfg<ASRC, NT>::kThreads, 1) tc_gemm_kernel(con
       const int ab = it & 1;
       if (!warp_wait(&accfull[ab], (it >> 1) & 1, p, abort_flag)) break;
       tc_fence_after();
-      // which issuers accumulated into this tile: with fewer stages than issuers, only the ones whose
-      // class a stage of the tile has (issuer j takes the stages g with g % G == j)
+      // which issuers accumulated into this tile: with one stage per tile only the one whose parity it has
       const int g0 = it * nk;
-      const int j0 = g0 % G;
-      const int ncols = mma_n(ti.nvalid, NT);   // accumulator columns the MMAs wrote
+      const bool use0 = C::kMmaGroups == 1 || nk >= 2 || (g0 & 1) == 0;
+      const bool use1 = C::kMmaGroups == 2 && (nk >= 2 || (g0 & 1) == 1);
 #pragma unroll
       for (int cb = 0; cb < NT; cb += 16) {
-        if (cb >= ncols) break;
         uint32_t v[16];
         __syncwarp();
-        bool have = false;
-#pragma unroll
-        for (int jm = 0; jm < G; ++jm) {
-          if (nk < G && (jm - j0 + G) % G >= nk) continue;   // issuer jm had no stage in this tile
+        if (use0) {
+          tmem_ld16(lane_base + C::kAccCol + ab * NT + cb, v);
+          tmem_wait_ld();
+        }
+        if (use1) {
           uint32_t v1[16];
-          tmem_ld16(lane_base + C::kAccCol + (jm * 2 + ab) * NT + cb, v1);
+          tmem_ld16(lane_base + C::kAccCol + (2 + ab) * NT + cb, v1);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            v[c] = have ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
-          have = true;
+            v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
         }
         if (OP == MOE_GEMM_GATEUP_SILU) {
           float u[16];
@@ -666,7 +632,7 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  tc_gemm_kernel<OP, ASRC, NT><<<grid, C::kThreads, C::kSmemBytes, s>>>(prm);
+  tc_gemm_kernel<OP, ASRC, NT><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -723,8 +689,8 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
       ok = make_map_2d(&prm.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.scales, p.K / 32, rows_total, p.K / 16, 8, 64,
                        CU_TENSOR_MAP_SWIZZLE_NONE);
   }
-  for (int k = 0; ok && k < 5 && (8 << k) <= nt; ++k)
-    ok = make_map_2d(&prm.tm_b[k], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.R, 2ull * p.K, KSUB, 8 << k,
+  if (ok)
+    ok = make_map_2d(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.R, 2ull * p.K, KSUB, nt,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   prm.scales = p.scales;
