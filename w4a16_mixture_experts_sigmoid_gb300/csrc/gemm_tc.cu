@@ -86,6 +86,7 @@ struct TcParams {
   uint16_t* out;
   int* status;
   int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
+  int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
   unsigned long long timeout_ns;
 };
 
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int e0 = 0; e0 < p.E; e0 += 32) {
         const int e = e0 + lane;
         const int cnt = (e < p.E) ? p.offsets[e + 1] - p.offsets[e] : 0;
-        const bool f = cnt > 0;
+        const bool f = cnt >= p.min_rows && cnt <= p.max_rows && cnt > 0;
         const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) : 0;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
         int incl = ntl;
@@ -702,6 +703,8 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.rows_per_expert = p.rows_per_expert;
   prm.out_cols = p.out_cols;
   prm.uniform_rows = p.uniform_rows;
+  prm.min_rows = p.min_rows;
+  prm.max_rows = p.max_rows;
   prm.rows_total = static_cast<int>(rows_total);
   prm.R = p.R;
   prm.out_mma_order = p.out_mma_order ? 1 : 0;

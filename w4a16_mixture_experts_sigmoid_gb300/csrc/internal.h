@@ -48,6 +48,8 @@ struct GemmProblem {
   int out_cols;            // I (gate/up) or H (down)
   int R;                   // rows of a and out
   int uniform_rows;        // >= 0: a single group of that many rows
+  int min_rows = 1;        // only experts with min_rows <= rows <= max_rows are computed
+  int max_rows = 1 << 30;
   bool a_mma_order;        // rows of a are stored in MMA K order
   bool out_mma_order;      // gate/up: write h in MMA K order
 };

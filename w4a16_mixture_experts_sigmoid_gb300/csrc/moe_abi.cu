@@ -152,6 +152,7 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
   if (flags & MOE_FLAG_GEMM_SIMT) return cuda_status(launch_gemm_simt(p, s));
   const int asrc = (flags & MOE_FLAG_A_SMEM) ? A_SMEM_DQ : A_TMEM_DQ;
   int nt = static_cast<int>((flags >> 8) & 0xFFu);
+  const bool auto_nt = nt == 0;
   if (nt == 0) {
     nt = auto_tokens_per_tile(p.R, d.E);
     if (asrc == A_SMEM_DQ && nt > 32) nt = 32;
@@ -163,7 +164,23 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
     p.a = scratch;
     p.a_mma_order = true;
   }
-  const cudaError_t e = launch_gemm_tc(p, asrc, nt, sms, s);
+  cudaError_t e;
+  if (auto_nt && nt == 128) {
+    // Many rows per expert on average, but skewed routing leaves a long tail of experts with a
+    // few rows, for which a 128-token tile is mostly padding: experts with up to 32 rows go to a
+    // launch with 32-token tiles, the rest to one with 128-token tiles. Each launch keeps only
+    // its experts, found from the offsets on the device.
+    GemmProblem small = p;
+    small.max_rows = 32;
+    e = launch_gemm_tc(small, asrc, 32, sms, s);
+    if (e == cudaSuccess) {
+      GemmProblem big = p;
+      big.min_rows = 33;
+      e = launch_gemm_tc(big, asrc, 128, sms, s);
+    }
+  } else {
+    e = launch_gemm_tc(p, asrc, nt, sms, s);
+  }
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(e);
 }
