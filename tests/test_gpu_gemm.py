@@ -150,3 +150,33 @@ def test_mma_order_rows_give_the_same_products(cuda_lib):
     B.moe_w4a16_grouped_gemm(0, d, w, dev(a_gu), T, dev(offsets), h0, ws, 0)
     B.moe_w4a16_grouped_gemm(0, d, w, dev(mma(a_gu)), T, dev(offsets), h1, ws, B.MOE_FLAG_ROWS_MMA_ORDER)
     assert torch.equal(dev(mma(h0.cpu().numpy())), h1)     # h comes back in the same K order
+
+
+def test_small_and_large_experts_split_between_launches(cuda_lib):
+    """With many rows per expert on average the GEMMs run one launch with 32-token tiles for the
+    experts with up to 32 rows and one with 128-token tiles for the rest: every row of both,
+    including experts right at the boundary and an empty one, matches the oracle."""
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    counts = np.array([1, 31, 32, 33, 64, 0, 128, 200], dtype=np.int64)    # mean 61 rows: 128-token choice
+    E, k, H, I = len(counts), 1, 256, 128
+    R = int(counts.sum())
+    T = R
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    layer = synth.make_layer(synth.LayerShape(E=E, top_k=k, H=H, I=I), seed=31)
+    a_gu = synth.normal_bf16((R, H), 1.0, 7, 102)
+    a_dn = synth.normal_bf16((R, I), 4.0, 7, 103)
+    ref_h = oracle.gateup_rows(a_gu, offsets, layer, range(R))
+    ref_y = oracle.down_rows(a_dn, offsets, layer, range(R))
+    d = B.dims(E, k, H, I)
+    tens = {key: dev(v) for key, v in layer.items()}
+    w = B.weights(tens["w13"], tens["s13"], tens["w2"], tens["s2"])
+    ws = torch.zeros(B.moe_workspace_size(d, T), dtype=torch.uint8, device="cuda")
+    off = dev(offsets)
+    h = torch.full((R, I), 0x7FC0, dtype=torch.int16, device="cuda")
+    y = torch.full((R, H), 0x7FC0, dtype=torch.int16, device="cuda")
+    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, d, w, dev(a_gu), T, off, h, ws, 0)
+    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(a_dn), T, off, y, ws, 0)
+    assert B.moe_check_status(ws) == B.MOE_OK
+    assert_close_h(bf16_dev_to_f32(h), ref_h, what="gate/up split")
+    assert_close_rms(bf16_dev_to_f32(y), ref_y, what="down split")
