@@ -83,3 +83,24 @@ def test_full_size_two_layer_stack_on_sampled_tokens(cuda_lib):
     whole = stack.forward(dev(x), [dev(v) for v in logits])
     assert stack.check_status() == 0
     assert np.array_equal(host(whole), host(chained))
+
+
+def test_tiny_stack_with_shared_experts_teacher_forced(cuda_lib):
+    """Layers with a bf16 shared expert: x + (routed + shared)(RMSNorm(x)), every layer."""
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer, MoeW4A16Stack
+    shape = synth.LayerShape(E=8, top_k=2, H=256, I=128, shared_I=128)
+    T, L = 12, 2
+    arrays = [synth.make_layer(shape, seed=40 + l) for l in range(L)]
+    layers = [MoeW4A16Layer.from_arrays(shape, a) for a in arrays]
+    logits = [synth.make_tokens(T, shape.H, shape.E, seed=40 + l)[1] for l in range(L)]
+    x, _ = synth.make_tokens(T, shape.H, shape.E, seed=40)
+    cur = dev(x)
+    for l in range(L):
+        one = MoeW4A16Stack([layers[l]])
+        nxt = one.forward(cur, [dev(logits[l])])
+        assert one.check_status() == 0
+        ref = oracle.stack_layer(host(cur, np.uint16), logits[l], arrays[l], shape.top_k, with_shared=True)
+        assert_close_rms(bf16_dev_to_f32(nxt), ref["out"], what=f"layer {l}")
+        cur = nxt
+    whole = MoeW4A16Stack(layers).forward(dev(x), [dev(v) for v in logits])
+    assert np.array_equal(host(whole), host(cur))

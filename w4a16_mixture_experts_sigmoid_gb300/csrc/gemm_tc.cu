@@ -119,6 +119,11 @@ struct Cfg {
   static constexpr int kWPeriod = (kWStages % 2 == 0) ? kWStages : 2 * kWStages;
   static constexpr int kBPeriod = (kBStages % 2 == 0) ? kBStages : 2 * kBStages;
   static constexpr int kAPeriod = (kNBuf % 2 == 0) ? kNBuf : 2 * kNBuf;
+  // A token-row slot is free once the MMAs of the stage that used it are done, which the same
+  // stage's A-buffer release already says. When kAPeriod >= kBStages the token-row producer waits
+  // for that release instead of a commit of its own (one commit per stage fewer for the issuers):
+  // the release's barrier cannot move on twice before the producer's next load, which it needs.
+  static constexpr bool kBViaA = kDq && kAPeriod >= kBStages;
   static constexpr int kMmaGroups = NT <= 64 ? 2 : 1;   // MMA issuers, each with its own accumulators
   static constexpr int kAccCol = (ASRC == A_TMEM_DQ) ? kNBuf * 128 : 0;
   static constexpr int kColsNeeded = kAccCol + 2 * kMmaGroups * NT;   // double-buffered per issuer
@@ -371,7 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int sbi = g % SB;
-          if (!mbar_wait(&bempty[sbi], ((g / SB) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) { ok = false; break; }
+          if (C::kBViaA) {
+            if (g >= SB) {
+              const int gn = g - SB + NB;   // the next user of the A buffer of stage g - SB
+              const int need = a_releases_needed(gn, NB, C::kAPeriod);
+              if (!mbar_wait(&aempty[(gn & 1) * NB + gn % NB], (need - 1) & 1, p.timeout_ns, abort_flag, p.status)) {
+                ok = false;
+                break;
+              }
+            }
+          } else if (!mbar_wait(&bempty[sbi], ((g / SB) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
           uint8_t* sb = bring + sbi * C::kBStage;
           uint64_t* bf = &bfull[(g & 1) * SB + sbi];
           mbar_arrive_expect_tx(bf, txb);
@@ -438,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             }
           }
           first = false;
-          mma_commit(&bempty[sbi]);
+          if (!C::kBViaA) mma_commit(&bempty[sbi]);
           if (C::kDq) mma_commit(&aempty[((g + NB) & 1) * NB + b]);   // to the group of the next user
           else mma_commit(&wempty[sw]);
         }
