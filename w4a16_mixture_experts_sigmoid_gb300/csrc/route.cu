@@ -60,9 +60,67 @@ __global__ void sigmoid_kernel(const float* __restrict__ x, int64_t n, float* __
 
 constexpr int kRouteWarps = 4;
 
+// One warp per token, k <= 32. Lane L owns experts L, L+32, ... (SLOTS of them, E <= 32 * SLOTS): all of
+// its logits are loaded first, so the loads overlap, then turned into scores in registers. Each
+// of the k rounds takes the best remaining score of every lane and a warp arg-max (lowest index
+// on ties); the winning lane marks its slot taken and broadcasts the raw score, which lane j keeps
+// for round j. The weights divide by the rank-order sum, accumulated one score at a time.
+template <int SLOTS>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel_reg(const float* __restrict__ logits, int T, int E,
+                                                                      int k, int32_t* __restrict__ ids,
+                                                                      float* __restrict__ wout) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRouteWarps + warp;
+  if (t >= T) return;
+  const float* lrow = logits + (int64_t)t * E;
+  float sc[SLOTS];
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) {
+    const int e = lane + 32 * i;
+    sc[i] = (e < E) ? __ldg(lrow + e) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < SLOTS; ++i) sc[i] = sigmoid_defined(sc[i]);
+  uint32_t taken = 0;  // bit i: expert lane + 32 i selected
+  float my_sel = 0.0f; // lane j < k: the score chosen in round j
+  for (int j = 0; j < k; ++j) {
+    float bk = -2.0f;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken & (1u << i))) {
+        const float kv = rank_key(sc[i]);
+        if (better(kv, e, bk, be)) { bk = kv; be = e; }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ok = __shfl_xor_sync(0xFFFFFFFFu, bk, off);
+      const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, off);
+      if (better(ok, oe, bk, be)) { bk = ok; be = oe; }
+    }
+    float sv = 0.0f;
+#pragma unroll
+    for (int i = 0; i < SLOTS; ++i)
+      if (lane + 32 * i == be) sv = sc[i];
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    sv = __shfl_sync(0xFFFFFFFFu, sv, be & 31);
+    if (lane == (j & 31)) my_sel = sv;
+    if (lane == 0) ids[(int64_t)t * k + j] = be;
+  }
+  float S = __shfl_sync(0xFFFFFFFFu, my_sel, 0);
+  for (int j = 1; j < k; ++j) S = __fadd_rn(S, __shfl_sync(0xFFFFFFFFu, my_sel, j));
+  if (lane < k) {
+    const float wj = (S == 0.0f) ? __fdiv_rn(1.0f, static_cast<float>(k)) : __fdiv_rn(my_sel, S);
+    wout[(int64_t)t * k + lane] = wj;
+  }
+}
+
+// Any k: scores in shared memory (the general path, used when k > 32).
 // One warp per token. Scores live in shared memory; lane L owns experts
 // L, L+32, ... and keeps a bit per owned expert once it is selected.
-__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(const float* __restrict__ logits, int T, int E,
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel_smem(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* __restrict__ ids,
                                                                   float* __restrict__ wout) {
   extern __shared__ float sm[];
@@ -121,9 +179,18 @@ cudaError_t launch_sigmoid(const float* logits, int64_t n, float* scores, cudaSt
 
 cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const size_t smem = sizeof(float) * kRouteWarps * (E + k);
   const unsigned blocks = static_cast<unsigned>((T + kRouteWarps - 1) / kRouteWarps);
-  route_kernel<<<blocks, kRouteWarps * 32, smem, s>>>(logits, T, E, k, ids, w);
+  const int slots = (E + 31) / 32;
+  if (k <= 32 && slots <= 32) {
+    if (slots <= 4) route_kernel_reg<4><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    else if (slots <= 8) route_kernel_reg<8><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    else if (slots <= 12) route_kernel_reg<12><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    else if (slots <= 16) route_kernel_reg<16><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    else route_kernel_reg<32><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+  } else {
+    const size_t smem = sizeof(float) * kRouteWarps * (E + k);
+    route_kernel_smem<<<blocks, kRouteWarps * 32, smem, s>>>(logits, T, E, k, ids, w);
+  }
   count_launches(1);
   return cudaGetLastError();
 }
