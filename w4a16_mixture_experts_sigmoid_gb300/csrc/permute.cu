@@ -8,8 +8,8 @@
 //   count   (one block per segment of kSeg assignments): per-segment histogram.
 //   scan    (one block): per-expert prefix over segments, then offsets[E+1].
 //   scatter (one block per segment): per-warp histograms and bases, then each
-//           warp walks its slice 32 assignments at a time in order, ranking
-//           equal ids with __match_any_sync.
+//           warp walks its slice (an eighth of the segment) 32 assignments at a
+//           time in order, ranking equal ids with __match_any_sync.
 #include "common.cuh"
 #include "internal.h"
 
@@ -88,9 +88,13 @@ __global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wb[i] = 0;
   __syncthreads();
-  constexpr int kSlice = kSeg / kScatterWarps;
-  const int64_t lo = (int64_t)blockIdx.x * kSeg + (int64_t)warp * kSlice;
-  const int64_t hi = min(Tk, lo + kSlice);
+  // warp w owns the w-th of eight contiguous slices of this block's segment (a multiple of 32
+  // assignments each, 512 for a full segment), so short batches keep every warp busy
+  const int64_t seg_lo = (int64_t)blockIdx.x * kSeg;
+  const int64_t seg_n = min((int64_t)kSeg, Tk - seg_lo);
+  const int64_t slice = ((seg_n + kScatterWarps - 1) / kScatterWarps + 31) / 32 * 32;
+  const int64_t lo = min(seg_lo + seg_n, seg_lo + (int64_t)warp * slice);
+  const int64_t hi = min(seg_lo + seg_n, lo + slice);
   for (int64_t i = lo + lane; i < hi; i += 32) {
     const int e = ids[i];
     if (e >= 0 && e < E) atomicAdd(&wb[warp * E + e], 1);
