@@ -36,14 +36,28 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const int p = inv[(int64_t)t * k + j];
-    if (p < 0) continue;
-    const float wj = w[(int64_t)t * k + j];
-    float f[8];
-    unpack8(__ldg(y + (int64_t)p * H8 + c), f);
+  // eight assignments at a time: their rows and weights are loaded before any is added, so the
+  // loads overlap; the sum still runs in rank order j
+  for (int j0 = 0; j0 < k; j0 += 8) {
+    int pj[8];
+    float wj[8];
+    uint4 yv[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u;
+      pj[u] = (j < k) ? __ldg(inv + (int64_t)t * k + j) : -1;
+      wj[u] = (j < k) ? __ldg(w + (int64_t)t * k + j) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) yv[u] = (pj[u] >= 0) ? __ldg(y + (int64_t)pj[u] * H8 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (pj[u] < 0) continue;
+      float f[8];
+      unpack8(yv[u], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], f[i], acc[i]);
+    }
   }
   if (addend != nullptr) {
     float f[8];

@@ -263,10 +263,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tpre[1] = n_wt * chunks;
       }
     } else {
+      // every expert's row count is loaded before the scan, so the loads overlap
+      int cnts[kMaxE / 32];
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c) {
+        const int e = 32 * c + lane;
+        cnts[c] = (e < p.E) ? __ldg(p.offsets + e + 1) - __ldg(p.offsets + e) : 0;
+      }
       int base_a = 0, base_t = 0;
-      for (int e0 = 0; e0 < p.E; e0 += 32) {
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c) {
+        const int e0 = 32 * c;
+        if (e0 >= p.E) break;
         const int e = e0 + lane;
-        const int cnt = (e < p.E) ? p.offsets[e + 1] - p.offsets[e] : 0;
+        const int cnt = cnts[c];
         const bool f = cnt >= p.min_rows && cnt <= p.max_rows && cnt > 0;
         const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) : 0;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
