@@ -87,6 +87,8 @@ struct TcParams {
   int* status;
   int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
   int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
+  int ksplit;              // K slices per tile (1: whole K); > 1 writes fp32 partial sums
+  float* partial;          // [ksplit][R][2][I] (gate/up) or [ksplit][R][H] (down), when ksplit > 1
   unsigned long long timeout_ns;
 };
 
@@ -144,6 +146,7 @@ struct TileInfo {
   int e;       // expert
   int row0;    // first token row of the chunk
   int nvalid;  // token rows of the chunk that belong to the expert
+  int split;   // K slice: stages [split * nk, (split + 1) * nk) of the whole K loop
 };
 
 __device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t* act_e, const int* tpre,
@@ -160,7 +163,9 @@ __device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t*
   if (p.uniform_rows >= 0) { start = 0; cnt = p.uniform_rows; }
   else { start = p.offsets[t.e]; cnt = p.offsets[t.e + 1] - start; }
   const int nch = (cnt + nt - 1) / nt;
-  const int rem = i - tpre[lo];
+  int rem = i - tpre[lo];
+  t.split = rem % p.ksplit;
+  rem /= p.ksplit;
   t.wt = rem / nch;
   const int c = rem - t.wt * nch;
   t.row0 = start + c * nt;
@@ -238,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = (OP == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
-  const int nk = (p.K + BK - 1) / BK;
+  const int nk = ((p.K + BK - 1) / BK) / p.ksplit;   // stages per tile (its K slice)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2 * SW; ++s) mbar_init(&wfull[s], 32);
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         *n_act_s = p.uniform_rows > 0 ? 1 : 0;
         act_e[0] = 0;
         tpre[0] = 0;
-        tpre[1] = n_wt * chunks;
+        tpre[1] = n_wt * chunks * p.ksplit;
       }
     } else {
       // every expert's row count is loaded before the scan, so the loads overlap
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int e = e0 + lane;
         const int cnt = cnts[c];
         const bool f = cnt >= p.min_rows && cnt <= p.max_rows && cnt > 0;
-        const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) : 0;
+        const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) * p.ksplit : 0;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
         int incl = ntl;
 #pragma unroll
@@ -320,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int grow_lo, grow_hi;
       if (OP == MOE_GEMM_GATEUP_SILU) { grow_lo = ebase + ti.wt * 64; grow_hi = ebase + p.out_cols + ti.wt * 64; }
       else { grow_lo = ebase + ti.wt * BM; grow_hi = grow_lo + 64; }
+      const int kb = ti.split * nk;   // first stage of this tile's K slice
       for (int ks = 0; ks < nk; ++ks, ++g) {
         const int sw = g % SW;
         uint64_t* wf = &wfull[(g & 1) * SW + sw];
@@ -333,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int grow = (r < 64) ? grow_lo + r : grow_hi + (r - 64);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const int gi = ks * 8 + q;
+              const int gi = (kb + ks) * 8 + q;
               uint16_t v = 0;
               if (gi < kg && grow < p.rows_total) v = p.scales[static_cast<int64_t>(grow) * kg + gi];
               sc[r * 8 + q] = v;
@@ -350,16 +356,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 int grow;
                 if (OP == MOE_GEMM_GATEUP_SILU) grow = (rb & 1) * p.out_cols + ti.wt * 64 + 16 * (rb >> 1);
                 else grow = ti.wt * BM + 16 * rb;
-                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, wf, ks * BK + sub * KSUB, grow,
+                tma_load_2d(sa + sub * (BM * 128) + rb * 2048, &p.tm_w, wf, (kb + ks) * BK + sub * KSUB, grow,
                             pol_w);
               }
             }
           } else {
-            tma_load_2d(sa, &p.tm_w, wf, ks * (BK / 8), grow_lo, pol_w);
-            tma_load_2d(sa + 64 * 128, &p.tm_w, wf, ks * (BK / 8), grow_hi, pol_w);
+            tma_load_2d(sa, &p.tm_w, wf, (kb + ks) * (BK / 8), grow_lo, pol_w);
+            tma_load_2d(sa + 64 * 128, &p.tm_w, wf, (kb + ks) * (BK / 8), grow_hi, pol_w);
             if (p.scale_tma) {
-              tma_load_2d(ss, &p.tm_s, wf, ks * 8, grow_lo, pol_w);
-              tma_load_2d(ss + 64 * 16, &p.tm_s, wf, ks * 8, grow_hi, pol_w);
+              tma_load_2d(ss, &p.tm_s, wf, (kb + ks) * 8, grow_lo, pol_w);
+              tma_load_2d(ss + 64 * 16, &p.tm_s, wf, (kb + ks) * 8, grow_hi, pol_w);
             }
           }
         } else {
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           mbar_arrive_expect_tx(bf, txb);
 #pragma unroll
           for (int sub = 0; sub < NSUB; ++sub)
-            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, bf, ks * BK + sub * KSUB, ti.row0, pol_b);
+            tma_load_2d(sb + sub * (NT * 128), &p.tm_b, bf, (ti.split * nk + ks) * BK + sub * KSUB, ti.row0, pol_b);
         }
       }
       for (int d = 0; d < SB && d < g; ++d) {
@@ -569,7 +575,32 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int c = 0; c < 16; ++c)
             v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
         }
-        if (OP == MOE_GEMM_GATEUP_SILU) {
+        if (p.ksplit > 1) {
+          // one K slice: its raw fp32 sums go to the partial buffer, each lane its own weight row
+          // (gate/up: lanes 0-15 the gate rows, 16-31 the up rows of the same outputs)
+          if (OP == MOE_GEMM_GATEUP_SILU) {
+            const int j = ti.wt * 64 + 16 * q + (lane & 15);
+            if (j < p.out_cols) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int row = ti.row0 + cb + c;
+                if (cb + c < ti.nvalid && row < p.R)
+                  p.partial[(static_cast<int64_t>(ti.split * p.R + row) * 2 + (lane >> 4)) * p.out_cols + j] =
+                      __uint_as_float(v[c]);
+              }
+            }
+          } else {
+            const int n = ti.wt * BM + l;
+            if (n < p.out_cols) {
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const int row = ti.row0 + cb + c;
+                if (cb + c < ti.nvalid && row < p.R)
+                  p.partial[static_cast<int64_t>(ti.split * p.R + row) * p.out_cols + n] = __uint_as_float(v[c]);
+              }
+            }
+          }
+        } else if (OP == MOE_GEMM_GATEUP_SILU) {
           float u[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) u[c] = __shfl_down_sync(0xFFFFFFFFu, __uint_as_float(v[c]), 16);
@@ -665,6 +696,30 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// After a launch with K slices: out[r][c] = bf16 of the finished sums, the slices added in order
+// (gate/up: SiLU(gate) * up, as the epilogue computes it; down: the plain sum).
+template <int OP>
+__global__ void __launch_bounds__(256) splitk_finish_kernel(const float* __restrict__ part, int S, int R, int cols,
+                                                            int out_mma_order, uint16_t* __restrict__ out) {
+  const int64_t n = static_cast<int64_t>(R) * cols;
+  for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += static_cast<int64_t>(gridDim.x) * 256) {
+    const int64_t row = i / cols;
+    const int col = static_cast<int>(i - row * cols);
+    float a = 0.0f, b = 0.0f;
+    for (int sl = 0; sl < S; ++sl) {
+      if (OP == MOE_GEMM_GATEUP_SILU) {
+        a += part[((static_cast<int64_t>(sl) * R + row) * 2) * cols + col];
+        b += part[((static_cast<int64_t>(sl) * R + row) * 2 + 1) * cols + col];
+      } else {
+        a += part[(static_cast<int64_t>(sl) * R + row) * cols + col];
+      }
+    }
+    const float v = (OP == MOE_GEMM_GATEUP_SILU) ? __fdividef(a, 1.0f + __expf(-a)) * b : a;
+    const int oc = (OP == MOE_GEMM_GATEUP_SILU && out_mma_order) ? mma_order_pos(col) : col;
+    out[row * cols + oc] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+}
+
 template <int OP>
 cudaError_t dispatch(const TcParams& prm, int asrc, int nt, int grid, cudaStream_t s) {
   switch (asrc) {
@@ -732,6 +787,10 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.uniform_rows = p.uniform_rows;
   prm.min_rows = p.min_rows;
   prm.max_rows = p.max_rows;
+  prm.ksplit = p.ksplit;
+  prm.partial = p.partial;
+  if (p.ksplit < 1 || ((p.K + BK - 1) / BK) % p.ksplit != 0 || (p.ksplit > 1 && p.partial == nullptr))
+    return cudaErrorInvalidValue;
   prm.rows_total = static_cast<int>(rows_total);
   prm.R = p.R;
   prm.out_mma_order = p.out_mma_order ? 1 : 0;
@@ -739,10 +798,20 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   // upper bound on tiles: every expert with rows contributes ceil(rows/nt) <= rows/nt + 1 chunks
   const int n_wt = (p.op == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
   const int64_t chunks = static_cast<int64_t>(p.R) / nt + (groups < p.R ? groups : p.R);
-  const int64_t tiles = chunks * n_wt;
+  const int64_t tiles = chunks * n_wt * p.ksplit;
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  if (p.op == MOE_GEMM_GATEUP_SILU) return dispatch<MOE_GEMM_GATEUP_SILU>(prm, asrc, nt, grid, s);
-  return dispatch<MOE_GEMM_DOWN>(prm, asrc, nt, grid, s);
+  cudaError_t e = (p.op == MOE_GEMM_GATEUP_SILU) ? dispatch<MOE_GEMM_GATEUP_SILU>(prm, asrc, nt, grid, s)
+                                                 : dispatch<MOE_GEMM_DOWN>(prm, asrc, nt, grid, s);
+  if (e != cudaSuccess || p.ksplit == 1) return e;
+  const int64_t n = static_cast<int64_t>(p.R) * p.out_cols;
+  const int fb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  if (p.op == MOE_GEMM_GATEUP_SILU)
+    splitk_finish_kernel<MOE_GEMM_GATEUP_SILU><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols,
+                                                                  p.out_mma_order ? 1 : 0, p.out);
+  else
+    splitk_finish_kernel<MOE_GEMM_DOWN><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols, 0, p.out);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

@@ -50,6 +50,8 @@ struct GemmProblem {
   int uniform_rows;        // >= 0: a single group of that many rows
   int min_rows = 1;        // only experts with min_rows <= rows <= max_rows are computed
   int max_rows = 1 << 30;
+  int ksplit = 1;          // K slices (divides the K stages); > 1 needs `partial`
+  float* partial = nullptr;  // fp32 [ksplit][R][2][out_cols] (gate/up) or [ksplit][R][out_cols]
   bool a_mma_order;        // rows of a are stored in MMA K order
   bool out_mma_order;      // gate/up: write h in MMA K order
 };

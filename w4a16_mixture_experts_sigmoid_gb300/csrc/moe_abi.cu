@@ -5,6 +5,7 @@
 #include "common.cuh"
 #include "internal.h"
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -23,6 +24,8 @@ using namespace moe;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxRows = int64_t(1) << 24;  // T * top_k
 constexpr int kMaxDim = 32768;                  // H, I, shared_I
+constexpr int kSplitMaxT = 256;                 // the shared expert splits K for T up to this
+constexpr int kMaxSplit = 8;                    // K slices at most
 
 struct DevInfo {
   int sms = 0;
@@ -83,7 +86,7 @@ moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 
 // Workspace layout of moe_forward (byte offsets, each 256-aligned).
 struct Layout {
-  size_t ids, w, offsets, sorted, inv, hist, xperm, h, y, hs, ys, end;
+  size_t ids, w, offsets, sorted, inv, hist, xperm, h, y, hs, ys, part, part_bytes, end;
 };
 
 Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
@@ -106,8 +109,25 @@ Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
   L.y = take(Tk * d.H * 2);
   L.hs = take(static_cast<size_t>(T) * shared_I * 2);
   L.ys = take(shared_I > 0 ? static_cast<size_t>(T) * d.H * 2 : 0);
+  // fp32 partial sums of the shared expert's K slices (small batches only)
+  L.part_bytes = shared_I > 0 && T <= kSplitMaxT
+                     ? static_cast<size_t>(kMaxSplit) * T * std::max(2 * shared_I, d.H) * 4 : 0;
+  L.part = take(L.part_bytes);
   L.end = off;
   return L;
+}
+
+// K slices for a launch with `tiles` tiles: the fewest that give every SM a tile, dividing the
+// `stages` of the K loop, at most kMaxSplit; 1 when the tiles already cover the SMs.
+int pick_ksplit(int64_t tiles, int stages, int sms) {
+  if (tiles >= sms) return 1;
+  int best = 1;
+  for (int d = 2; d <= kMaxSplit && d <= stages; ++d) {
+    if (stages % d) continue;
+    best = d;
+    if (tiles * d >= sms) break;
+  }
+  return best;
 }
 
 int auto_tokens_per_tile(int64_t rows, int groups) {
@@ -185,8 +205,12 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
   return cuda_status(e);
 }
 
+// The dense shared expert. Its weights make only 2*Is/128 gate/up and H/128 down tiles, fewer
+// than the SMs when a small batch fills one token tile; then each GEMM splits its K loop into
+// slices (fp32 partial sums in `part`, finished by a second kernel) so that every SM streams
+// weights. part may be null (no split).
 moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* hs,
-                        uint16_t* out, int* status, uint32_t flags, int sms, cudaStream_t s) {
+                        uint16_t* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
   const int Is = w->shared_I;
   GemmProblem p;
   p.bf16_weights = true;
@@ -207,6 +231,12 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   p.rows_per_expert = 2 * Is;
   p.out_cols = Is;
   const int nt = T <= 16 ? 16 : (T <= 32 ? 32 : 64);
+  const bool split = part != nullptr && T <= kSplitMaxT && !(flags & MOE_FLAG_GEMM_SIMT);
+  const int64_t chunks = (T + nt - 1) / nt;
+  if (split) {
+    p.ksplit = pick_ksplit(chunks * (Is / 64), (d.H + 255) / 256, sms);
+    p.partial = part;
+  }
   cudaError_t e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
   // down: hs [T][Is] -> out [T][H]
@@ -217,6 +247,7 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   p.K = Is;
   p.rows_per_expert = d.H;
   p.out_cols = d.H;
+  if (split) p.ksplit = pick_ksplit(chunks * ((d.H + 127) / 128), (Is + 255) / 256, sms);
   e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
   return MOE_OK;
@@ -253,7 +284,8 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
   if (w->shared_wgu != nullptr) {
     uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
     uint16_t* ys = reinterpret_cast<uint16_t*>(ws + L.ys);
-    st = run_shared(d, w, x, T, hs, ys, status, flags, sms, s);
+    float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
+    st = run_shared(d, w, x, T, hs, ys, status, flags, sms, part, s);
     if (st != MOE_OK) return st;
     addend = ys;
   }
@@ -380,8 +412,9 @@ moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint1
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(w8 + L.part) : nullptr;
   return run_shared(d, w, x, T, reinterpret_cast<uint16_t*>(w8 + L.hs), out, reinterpret_cast<int*>(w8), flags,
-                    di.sms, as_stream(stream));
+                    di.sms, part, as_stream(stream));
 }
 
 moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w, int32_t T, int32_t k,
