@@ -52,3 +52,17 @@ def test_reference_arm_prints_nothing_off_rank_0(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.run_reference(argparse.Namespace(workload="tiny", steps=2, warmup=1, gpus=2))
     assert capsys.readouterr().out == ""
+
+
+def test_kernel_roofline_takes_the_slower_roof():
+    import bench
+    hbm, tc = 6788.6, 1722.1
+    # a decode-shaped gate/up launch: 291 experts' weights, 512 rows -> bytes dominate
+    dec = bench.kernel_roofline("gemm_gate_up", 4.815e9, 2.0 * 512 * 7168 * 4096, 1.1, None, hbm, tc, "measured")
+    assert dec["bound"] == "hbm" and dec["unit"] == "GB/s"
+    assert dec["frac"] == pytest.approx(4.815e9 / 1.1e-3 / 1e9 / hbm)
+    # a prefill-shaped one: 32768 rows over 384 experts -> flops dominate
+    fl = 2.0 * 32768 * 7168 * 4096
+    pre = bench.kernel_roofline("gemm_gate_up", 6.946e9, fl, 2.72, None, hbm, tc, "measured")
+    assert pre["bound"] == "tensor" and pre["unit"] == "TFLOP/s" and pre["peak"] == tc
+    assert pre["frac"] == pytest.approx(fl / 2.72e-3 / 1e12 / tc)

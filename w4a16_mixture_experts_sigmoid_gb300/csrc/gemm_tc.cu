@@ -87,7 +87,7 @@ struct TcParams {
   int* status;
   int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
   int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
-  int ksplit;              // K slices per tile (1: whole K); > 1 writes fp32 partial sums
+  int ksplit;              // K slices per tile (1: whole K); > 1 (bf16 weights only) writes fp32 partial sums
   float* partial;          // [ksplit][R][2][I] (gate/up) or [ksplit][R][H] (down), when ksplit > 1
   unsigned long long timeout_ns;
 };
@@ -150,7 +150,7 @@ struct TileInfo {
 };
 
 __device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t* act_e, const int* tpre,
-                                                const TcParams& p, int nt) {
+                                                const TcParams& p, int nt, int ksplit) {
   int lo = 0, hi = n_act - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -164,8 +164,11 @@ __device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t*
   else { start = p.offsets[t.e]; cnt = p.offsets[t.e + 1] - start; }
   const int nch = (cnt + nt - 1) / nt;
   int rem = i - tpre[lo];
-  t.split = rem % p.ksplit;
-  rem /= p.ksplit;
+  t.split = 0;
+  if (ksplit > 1) {
+    t.split = rem % ksplit;
+    rem /= ksplit;
+  }
   t.wt = rem / nch;
   const int c = rem - t.wt * nch;
   t.row0 = start + c * nt;
@@ -243,7 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = (OP == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
-  const int nk = ((p.K + BK - 1) / BK) / p.ksplit;   // stages per tile (its K slice)
+  // K slices exist only for the dense bf16 weights (the shared expert); the int4 kernels are
+  // compiled without them: the slice arithmetic and the partial-sum epilogue cost the routed
+  // GEMMs 1-4% when present.
+  const int ksplit = (ASRC == A_SMEM_BF16) ? p.ksplit : 1;
+  const int nk = ((p.K + BK - 1) / BK) / ksplit;   // stages per tile (its K slice)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2 * SW; ++s) mbar_init(&wfull[s], 32);
@@ -265,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         *n_act_s = p.uniform_rows > 0 ? 1 : 0;
         act_e[0] = 0;
         tpre[0] = 0;
-        tpre[1] = n_wt * chunks * p.ksplit;
+        tpre[1] = n_wt * chunks * ksplit;
       }
     } else {
       // every expert's row count is loaded before the scan, so the loads overlap
@@ -283,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int e = e0 + lane;
         const int cnt = cnts[c];
         const bool f = cnt >= p.min_rows && cnt <= p.max_rows && cnt > 0;
-        const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) * p.ksplit : 0;
+        const int ntl = f ? n_wt * ((cnt + NT - 1) / NT) * ksplit : 0;
         const unsigned m = __ballot_sync(0xFFFFFFFFu, f);
         int incl = ntl;
 #pragma unroll
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int g = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT, ksplit);
       const int ebase = ti.e * p.rows_per_expert;
       int grow_lo, grow_hi;
       if (OP == MOE_GEMM_GATEUP_SILU) { grow_lo = ebase + ti.wt * 64; grow_hi = ebase + p.out_cols + ti.wt * 64; }
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int g = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x) {
-        const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+        const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT, ksplit);
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int sbi = g % SB;
           if (C::kBViaA) {
@@ -551,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     int it = 0;
     for (int i = blockIdx.x; i < total; i += gridDim.x, ++it) {
-      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT);
+      const TileInfo ti = decode_tile(i, n_act, act_e, tpre, p, NT, ksplit);
       const int ab = it & 1;
       if (!warp_wait(&accfull[ab], (it >> 1) & 1, p, abort_flag)) break;
       tc_fence_after();
@@ -575,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int c = 0; c < 16; ++c)
             v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
         }
-        if (p.ksplit > 1) {
+        if (ASRC == A_SMEM_BF16 && ksplit > 1) {
           // one K slice: its raw fp32 sums go to the partial buffer, each lane its own weight row
           // (gate/up: lanes 0-15 the gate rows, 16-31 the up rows of the same outputs)
           if (OP == MOE_GEMM_GATEUP_SILU) {
@@ -789,7 +796,8 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.max_rows = p.max_rows;
   prm.ksplit = p.ksplit;
   prm.partial = p.partial;
-  if (p.ksplit < 1 || ((p.K + BK - 1) / BK) % p.ksplit != 0 || (p.ksplit > 1 && p.partial == nullptr))
+  if (p.ksplit < 1 || ((p.K + BK - 1) / BK) % p.ksplit != 0 || (p.ksplit > 1 && p.partial == nullptr) ||
+      (p.ksplit > 1 && !p.bf16_weights))
     return cudaErrorInvalidValue;
   prm.rows_total = static_cast<int>(rows_total);
   prm.R = p.R;
