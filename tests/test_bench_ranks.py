@@ -66,3 +66,25 @@ def test_kernel_roofline_takes_the_slower_roof():
     pre = bench.kernel_roofline("gemm_gate_up", 6.946e9, fl, 2.72, None, hbm, tc, "measured")
     assert pre["bound"] == "tensor" and pre["unit"] == "TFLOP/s" and pre["peak"] == tc
     assert pre["frac"] == pytest.approx(fl / 2.72e-3 / 1e12 / tc)
+
+
+def test_profile_traffic_only_for_the_captured_source(monkeypatch, tmp_path):
+    """`roofline.traffic` comes from a committed ncu summary only while the kernel source still
+    hashes to the one the summary was captured from."""
+    import bench
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    sha = bench.kernel_source_sha()
+    (prof / "gemm_gate_up_w1.md").write_text(f"source_sha256: {sha}\ndram_bytes_per_launch: 4.8e9\n")
+    (prof / "gemm_gate_up_w2.md").write_text(f"source_sha256: {'0' * 64}\ndram_bytes_per_launch: 4.8e9\n")
+    (prof / "gemm_gate_up_w3.md").write_text(f"source_sha256: {sha}\n")
+    real_root = bench.ROOT
+    csrc = tmp_path / "w4a16_mixture_experts_sigmoid_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("gemm_tc.cu", "common.cuh"):
+        (csrc / f).write_bytes(open(f"{real_root}/w4a16_mixture_experts_sigmoid_gb300/csrc/{f}", "rb").read())
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profile_traffic("gemm_gate_up", "w1") == 4.8e9
+    assert bench.profile_traffic("gemm_gate_up", "w2") is None       # another kernel source
+    assert bench.profile_traffic("gemm_gate_up", "w3") is None       # no byte count
+    assert bench.profile_traffic("gemm_gate_up", "absent") is None
