@@ -515,6 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           uint4 wv[4];
 #pragma unroll
           for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
+          // The first half row's conversion needs no A buffer, so for gate/up it runs before the
+          // wait for one (gate/up 3% faster at decode; the same for down made it 2% slower).
+          constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
+          uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
+#pragma unroll
+          for (int c = 0; c < kPreChunks; ++c)
+            dequant_group(wv[c], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), pre[c]);
           if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -529,8 +536,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
               const int c = half * 4 + cc;
-              uint32_t dq[16];
-              dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dq);
+              uint32_t dqc[16];
+              if (c >= kPreChunks)
+                dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dqc);
+              const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
               if (ASRC == A_TMEM_DQ) {
                 tmem_st8(lane_base + b * 128 + c * 16, dq);
                 tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
