@@ -120,7 +120,11 @@ MOE_API const char* moe_status_string(moe_status_t s);
  * Before its first use the first 256 bytes of a workspace must be zero. */
 MOE_API size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags);
 
-/* Step 1, routing. logits fp32 [T][E] -> topk_ids int32 [T][k] and topk_w fp32
+/* Step 1, routing. Passage: "feat(pytorch): support Kimi K2.6", Motivation and
+ * Changes ("MoE routing"); "Kimi-K2.6" catalog page, GEOMETRY ("384 routed
+ * experts, 8 per token"). The pages name routing but not its function; the
+ * sigmoid / top-k / renormalise reading is the one stated at the top.
+ * logits fp32 [T][E] -> topk_ids int32 [T][k] and topk_w fp32
  * [T][k], in rank order (score descending, expert index ascending on ties).
  * score = 1 / (1 + e(-logit)), every operation one IEEE fp32 operation rounded
  * to nearest even, with e(t) = p(r) * 2^n, n = rint(t * log2 e),
@@ -135,7 +139,11 @@ MOE_API moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_
 /* The router's score function alone, element-wise: scores[i] = score(logits[i]). */
 MOE_API moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream);
 
-/* Step 2, expert-sorted permutation. Assignment i = t*k + j goes to row
+/* Step 2, expert-sorted permutation. Passage: "Kimi-K2.6" catalog page,
+ * GEOMETRY (8 of 384 experts per token) and "feat(pytorch): support Kimi
+ * K2.6", Changes (W4A16 MoE kernels). The pages print no permutation: this
+ * step is the design choice that groups each expert's rows so its int4
+ * weights are read once per batch by one grouped GEMM. Assignment i = t*k + j goes to row
  * inv_perm[i]; rows are grouped by expert, expert e owning rows
  * [expert_offsets[e], expert_offsets[e+1]), and within an expert ordered by
  * increasing i (a stable sort). sorted_token_ids[row] = the row's token.
@@ -177,7 +185,10 @@ MOE_API moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, 
  * Set-up: the first call on a device, with that device current, looks up the
  * array's device address (this can load the library's module onto the
  * device) and checks the device; make that first call before any stream
- * capture. Later calls on the device only launch kernels.
+ * capture. Later calls on the device only launch kernels. A set-up that
+ * failed (MOE_ERR_CUDA, for instance inside a capture) is not remembered:
+ * the next call on that device tries again. MOE_ERR_UNSUPPORTED_DEVICE is
+ * final for that device.
  *
  * Every call on a device uses the same array: calls whose kernels overlap on
  * the GPU (other streams, other host threads, without ordering between them)
@@ -189,7 +200,12 @@ MOE_API moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, int32_t
                                         uint16_t* x_perm, int32_t* status, uint32_t flags,
                                         void* stream);
 
-/* Steps 3 and 4, the grouped W4A16 GEMMs over expert-sorted rows. Row r of
+/* Steps 3 and 4, the grouped W4A16 GEMMs over expert-sorted rows. Passage:
+ * "Kimi-K2.6" catalog page, QUANT and PARAMS (INT4 via compressed-tensors,
+ * group size 32, pack-quantized, symmetric, int4 weights in int32 containers)
+ * and GEOMETRY (hidden 7168, moe_intermediate_size 2048; three H x I matrices
+ * per expert by the I32 parameter count); "feat(pytorch): support Kimi
+ * K2.6", Changes ("compressed-tensors W4A16 MoE"). Row r of
  * a_rows (bf16 [R][K], R = T*k) belongs to the expert e with
  * expert_offsets[e] <= r < expert_offsets[e+1]. Each weight is dequantised as
  * bf16(q * scale) and the products accumulate in fp32 on the tensor cores.
@@ -207,20 +223,31 @@ MOE_API moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_
                                     const int32_t* expert_offsets, uint16_t* out_rows,
                                     void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
-/* The dense bf16 shared expert: out bf16 [T][H] = Wd (SiLU(Wg x) .* (Wu x)) for
+/* The dense bf16 shared expert. Passage: "Kimi-K2.6" catalog page, GEOMETRY
+ * (n_shared_experts 1, moe_intermediate_size 2048) and PARAMS (the BF16
+ * share of the checkpoint, outside the INT4 bank).
+ * out bf16 [T][H] = Wd (SiLU(Wg x) .* (Wu x)) for
  * x bf16 [T][H], fp32 accumulation. Needs w->shared_wgu, w->shared_wd, and
  * moe_workspace_size(d, T, w->shared_I, flags) bytes of workspace. */
 MOE_API moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T,
                                uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
-/* Step 5, combine: out[t] = bf16( sum_j topk_w[t][j] * y[inv_perm[t*k+j]]
+/* Step 5, combine. Passage: "Kimi-K2.6" catalog page, GEOMETRY (8 routed
+ * experts plus one shared expert per token, summed into one output);
+ * "feat(pytorch): support Kimi K2.6", Changes ("MoE routing": the routing
+ * weights scale the experts' outputs).
+ * out[t] = bf16( sum_j topk_w[t][j] * y[inv_perm[t*k+j]]
  * (+ addend[t]) ), fp32 accumulation in rank order j, one rounding at the end.
  * y_rows bf16 [T*k][H], addend bf16 [T][H] or NULL, out bf16 [T][H]. */
 MOE_API moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w,
                          int32_t T, int32_t k, int32_t H, const uint16_t* addend,
                          uint16_t* out, void* stream);
 
-/* The whole layer: route, permute (with gather), gate/up GEMM, down GEMM,
+/* The whole layer. Passage: "feat(pytorch): support Kimi K2.6", Motivation
+ * and Changes (the compressed-tensors W4A16 MoE with its routing) and
+ * "Kimi-K2.6" catalog page, GEOMETRY/QUANT (384 INT4 routed experts, 8 per
+ * token, one higher-precision shared expert).
+ * Route, permute (with gather), gate/up GEMM, down GEMM,
  * the shared expert when w has one, combine.
  *   x bf16 [T][H], logits fp32 [T][E] -> out bf16 [T][H].
  * ws_bytes >= moe_workspace_size(d, T, w->shared_I, flags). */

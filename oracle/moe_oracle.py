@@ -182,11 +182,22 @@ def permute(ids: np.ndarray, E: int):
 # Weight format
 # ---------------------------------------------------------------------------
 
+# Byte b of a little-endian word holds two inputs: bits 0..3 the earlier one,
+# bits 4..7 the next. This table lists (q_low, q_high) = (nibble - 8) for all
+# 256 byte values, so unpacking is one table lookup per byte.
+_BYTE_TO_Q = np.array([[(b & 15) - 8, (b >> 4) - 8] for b in range(256)], dtype=np.int8)
+_BYTE_TO_QF = _BYTE_TO_Q.astype(np.float32)
+
+
+def _word_bytes(words: np.ndarray) -> np.ndarray:
+    """int32 words [..., W] -> their bytes [..., 4W], least significant byte of each word first."""
+    return np.ascontiguousarray(np.asarray(words).astype("<u4", copy=False)).view(np.uint8)
+
+
 def unpack_int4(words: np.ndarray) -> np.ndarray:
     """int32 words [..., W] -> signed int4 values [..., 8W] (input 8c+j from bits 4j..4j+3)."""
-    u = np.asarray(words).view(np.uint32)
-    nib = np.stack([(u >> np.uint32(4 * j)) & np.uint32(15) for j in range(8)], axis=-1)
-    return (nib.astype(np.int16) - 8).reshape(*u.shape[:-1], u.shape[-1] * 8).astype(np.int8)
+    b = _word_bytes(words)
+    return _BYTE_TO_Q[b].reshape(*b.shape[:-1], b.shape[-1] * 2)
 
 
 def pack_int4(q: np.ndarray) -> np.ndarray:
@@ -202,9 +213,11 @@ def pack_int4(q: np.ndarray) -> np.ndarray:
 
 def dequant(words: np.ndarray, scale_bits: np.ndarray, group: int = 32) -> np.ndarray:
     """W[n, i] = q[n, i] * scale[n, i // group], in fp32 (exact: 4-bit x 8-bit significands)."""
-    q = unpack_int4(words).astype(np.float32)
-    s = bf16_to_f32(scale_bits)
-    return (q * np.repeat(s, group, axis=-1)).astype(np.float32)
+    b = _word_bytes(words)
+    q = _BYTE_TO_QF[b].reshape(*b.shape[:-1], -1, group)       # [..., groups, group]
+    s = bf16_to_f32(scale_bits)[..., None]                     # [..., groups, 1]
+    q *= s
+    return q.reshape(*b.shape[:-1], b.shape[-1] * 2)
 
 
 def expert_int4_params(H: int, I: int) -> int:
@@ -223,21 +236,44 @@ def silu(v: np.ndarray) -> np.ndarray:
 
 
 def expert_mlp(x: np.ndarray, w13: np.ndarray, s13: np.ndarray, w2: np.ndarray, s2: np.ndarray) -> np.ndarray:
-    """One routed expert on one token: fp32 x [H] -> fp32 y [H]."""
+    """One routed expert: fp32 x [H] (one token) -> fp32 y [H], or x [n, H] -> y [n, H] (each row on its own).
+
+    Dequantise W13 and W2 to fp32, then per token g, u = W13 x (gate rows
+    first), h = SiLU(g) * u, y = W2 h. Several tokens only put several
+    columns into the same matrix products.
+    """
     I = w2.shape[-1] * 8
+    X = np.asarray(x, dtype=np.float32)
+    single = X.ndim == 1
+    X = X.reshape(-1, X.shape[-1])
     W13 = dequant(w13, s13)                  # [2I, H]
-    gu = W13 @ np.asarray(x, dtype=np.float32)
-    h = (silu(gu[:I]) * gu[I:]).astype(np.float32)
+    gu = (X @ W13.T).astype(np.float32)      # row t: W13 x_t
+    h = (silu(gu[:, :I]) * gu[:, I:]).astype(np.float32)
     W2 = dequant(w2, s2)                     # [H, I]
-    return (W2 @ h).astype(np.float32)
+    y = (h @ W2.T).astype(np.float32)
+    return y[0] if single else y
 
 
 def shared_expert(x: np.ndarray, wgu_bits: np.ndarray, wd_bits: np.ndarray) -> np.ndarray:
-    """The bf16 shared expert on one token (gate rows first in wgu): fp32 [H] -> fp32 [H]."""
+    """The bf16 shared expert (gate rows first in wgu): fp32 x [H] -> fp32 [H], or [n, H] -> [n, H]."""
     Is = wd_bits.shape[1]
-    gu = bf16_to_f32(wgu_bits) @ np.asarray(x, dtype=np.float32)
-    h = (silu(gu[:Is]) * gu[Is:]).astype(np.float32)
-    return (bf16_to_f32(wd_bits) @ h).astype(np.float32)
+    X = np.asarray(x, dtype=np.float32)
+    single = X.ndim == 1
+    X = X.reshape(-1, X.shape[-1])
+    gu = (X @ bf16_to_f32(wgu_bits).T).astype(np.float32)
+    h = (silu(gu[:, :Is]) * gu[:, Is:]).astype(np.float32)
+    y = (h @ bf16_to_f32(wd_bits).T).astype(np.float32)
+    return y[0] if single else y
+
+
+def _map(fn, items, workers: int):
+    """fn over items, on a thread pool when workers > 1 (numpy and BLAS release the GIL)."""
+    items = list(items)
+    if workers <= 1 or len(items) <= 1:
+        return [fn(i) for i in items]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(min(workers, len(items))) as ex:
+        return list(ex.map(fn, items))
 
 
 def combine(y_rows: np.ndarray, inv: np.ndarray, w: np.ndarray, addend: np.ndarray | None = None) -> np.ndarray:
@@ -253,11 +289,15 @@ def combine(y_rows: np.ndarray, inv: np.ndarray, w: np.ndarray, addend: np.ndarr
 
 
 def moe_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, tokens=None,
-              with_shared: bool = False) -> dict:
+              with_shared: bool = False, workers: int = 1) -> dict:
     """The routed MoE layer: routing for every token, outputs for ``tokens``.
 
     Returns ids, weights, offsets, sorted_token_ids, inv_perm (all tokens) and
-    ``out`` fp32 [len(tokens), H] for the requested tokens (all by default).
+    ``out`` fp32 [len(tokens), H] for the requested tokens (all by default):
+    out[t] = sum over rank j of w[t, j] * expert_{ids[t, j]}(x[t]), summed in
+    rank order, plus the shared expert when asked. Each expert is dequantised
+    once and applied to every requested token that selected it; ``workers``
+    threads run different experts at the same time.
     """
     T = x_bits.shape[0]
     E = layer["w13"].shape[0]
@@ -265,17 +305,20 @@ def moe_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, token
     offsets, sorted_ids, inv = permute(ids, E)
     tokens = np.arange(T) if tokens is None else np.asarray(tokens)
     H = x_bits.shape[1]
+    X = bf16_to_f32(x_bits[tokens])                  # [n, H]
+    sel = ids[tokens]                                # [n, k]
+    y = np.zeros((len(tokens), k, H), dtype=np.float32)
+
+    def one_expert(e):
+        r, j = np.nonzero(sel == e)
+        y[r, j] = expert_mlp(X[r], layer["w13"][e], layer["s13"][e], layer["w2"][e], layer["s2"][e])
+
+    _map(one_expert, np.unique(sel), workers)
     out = np.zeros((len(tokens), H), dtype=np.float32)
-    for r, t in enumerate(tokens):
-        x = bf16_to_f32(x_bits[t])
-        acc = np.zeros(H, dtype=np.float32)
-        for j in range(k):
-            e = int(ids[t, j])
-            y = expert_mlp(x, layer["w13"][e], layer["s13"][e], layer["w2"][e], layer["s2"][e])
-            acc = (acc + w[t, j] * y).astype(np.float32)
-        if with_shared:
-            acc = (acc + shared_expert(x, layer["sh_gu"], layer["sh_d"])).astype(np.float32)
-        out[r] = acc
+    for j in range(k):
+        out = (out + w[tokens, j:j + 1] * y[:, j]).astype(np.float32)
+    if with_shared:
+        out = (out + shared_expert(X, layer["sh_gu"], layer["sh_d"])).astype(np.float32)
     return {"ids": ids, "weights": w, "offsets": offsets, "sorted_token_ids": sorted_ids,
             "inv_perm": inv, "out": out, "tokens": tokens}
 
@@ -285,27 +328,40 @@ def moe_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, token
 # ---------------------------------------------------------------------------
 
 def _expert_of_rows(offsets: np.ndarray, rows) -> np.ndarray:
+    """Expert e of each row r: offsets[e] <= r < offsets[e + 1] (empty experts own no row)."""
     return np.searchsorted(np.asarray(offsets), np.asarray(rows), side="right") - 1
 
 
-def gateup_rows(a_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows) -> np.ndarray:
+def gateup_rows(a_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows, workers: int = 1) -> np.ndarray:
     """h = SiLU(W_gate x) * (W_up x) for expert-sorted activation rows ``rows`` -> fp32 [len(rows), I]."""
     I = layer["w2"].shape[-1] * 8
-    out = []
-    for p, e in zip(rows, _expert_of_rows(offsets, rows)):
+    rows = np.asarray(list(rows), dtype=np.int64)
+    owner = _expert_of_rows(offsets, rows)
+    out = np.zeros((len(rows), I), dtype=np.float32)
+
+    def one_expert(e):
+        sel = np.nonzero(owner == e)[0]
         W13 = dequant(layer["w13"][e], layer["s13"][e])
-        gu = W13 @ bf16_to_f32(a_bits[p])
-        out.append(silu(gu[:I]) * gu[I:])
-    return np.asarray(out, dtype=np.float32).reshape(len(out), I)
+        gu = (bf16_to_f32(a_bits[rows[sel]]) @ W13.T).astype(np.float32)
+        out[sel] = silu(gu[:, :I]) * gu[:, I:]
+
+    _map(one_expert, np.unique(owner), workers)
+    return out
 
 
-def down_rows(h_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows) -> np.ndarray:
+def down_rows(h_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows, workers: int = 1) -> np.ndarray:
     """y = W2 h for expert-sorted rows ``rows`` -> fp32 [len(rows), H]."""
     H = layer["w2"].shape[1]
-    out = []
-    for p, e in zip(rows, _expert_of_rows(offsets, rows)):
-        out.append(dequant(layer["w2"][e], layer["s2"][e]) @ bf16_to_f32(h_bits[p]))
-    return np.asarray(out, dtype=np.float32).reshape(len(out), H)
+    rows = np.asarray(list(rows), dtype=np.int64)
+    owner = _expert_of_rows(offsets, rows)
+    out = np.zeros((len(rows), H), dtype=np.float32)
+
+    def one_expert(e):
+        sel = np.nonzero(owner == e)[0]
+        out[sel] = bf16_to_f32(h_bits[rows[sel]]) @ dequant(layer["w2"][e], layer["s2"][e]).T
+
+    _map(one_expert, np.unique(owner), workers)
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -320,7 +376,7 @@ def rmsnorm(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
 
 
 def stack_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, eps: float = 1e-6, tokens=None,
-                with_shared: bool = False) -> dict:
+                with_shared: bool = False, workers: int = 1) -> dict:
     """One block of the layer stack, x + MoE(RMSNorm(x)), for ``tokens`` (all by default).
 
     The pages give 60 MoE layers ("Kimi-K2.6", GEOMETRY) but not how they are
@@ -330,7 +386,7 @@ def stack_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, eps
     ``out`` = x + MoE(...) in fp32.
     """
     xn_bits = f32_to_bf16(rmsnorm(bf16_to_f32(x_bits), eps))
-    res = moe_layer(xn_bits, logits, layer, k, tokens=tokens, with_shared=with_shared)
+    res = moe_layer(xn_bits, logits, layer, k, tokens=tokens, with_shared=with_shared, workers=workers)
     res["out"] = (bf16_to_f32(x_bits[res["tokens"]]) + res["out"]).astype(np.float32)
     res["xn_bits"] = xn_bits
     return res

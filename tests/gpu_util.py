@@ -51,12 +51,51 @@ def assert_close_rms(got, ref, max_rel=MAX_REL, mean_rel=MEAN_REL, what=""):
 # weight rounding of g and u (relative 2^-9 per weight, ~2^-9/sqrt(3) of a
 # K-term dot product's size), multiplied by the other factor, so it scales with
 # |g| and |u| rather than with |h|. Emulating exactly that arithmetic on the CPU
-# (bf16 weights, exact accumulation, bf16 output) gives max |err| up to
-# 0.053 RMS(h) on the test shapes, mean 0.0015 RMS; the bound for h is
-# 8e-2 RMS max (1.5x that), 5e-3 RMS mean. The down rows y = W2 h are near
-# Gaussian and keep the layer's own bound (emulated max 0.017 RMS).
+# (bf16 weights, exact accumulation, bf16 output) on the GEMM test problems
+# below reaches max |err| ~0.05 RMS(h); tests/test_tolerance_emulation.py
+# recomputes that figure and checks this bound keeps a 1.5x margin over it.
+# The down rows y = W2 h are near Gaussian and keep the layer's own bound.
 H_MAX_REL = 8e-2
+H_MARGIN = 1.5
 
 
 def assert_close_h(got, ref, what=""):
     assert_close_rms(got, ref, max_rel=H_MAX_REL, mean_rel=MEAN_REL, what=what)
+
+
+# ---------------------------------------------------------------------------
+# grouped-GEMM test problems: (E, k, H, I, T, skew), shapes that span several
+# tiles and ragged tails. Shared by the GPU GEMM tests and the CPU emulation
+# of the tolerance above (no GPU needed to build them).
+# ---------------------------------------------------------------------------
+GEMM_SHAPES = [
+    (8, 2, 256, 128, 16, None),        # the tiny layer
+    (5, 3, 288, 96, 37, None),         # K tails: H % 256 != 0, I % 64 != 0
+    (3, 2, 512, 256, 200, None),       # several token chunks per expert
+    (1, 1, 1024, 512, 300, None),      # one expert owns every row
+    (16, 4, 2048, 1024, 64, "half"),   # deep K, empty experts
+]
+
+_gemm_cache = {}
+
+
+def gemm_problem(E, k, H, I, T, skew):
+    """Seeded weights, routing offsets and activation rows of one GEMM test problem,
+    with the oracle's h and y for every row."""
+    import oracle
+    import synth
+    key = (E, k, H, I, T, skew)
+    if key not in _gemm_cache:
+        layer = synth.make_layer(synth.LayerShape(E=E, top_k=k, H=H, I=I), seed=E + H)
+        logits = np.random.default_rng(T).standard_normal((T, E)).astype(np.float32)
+        if skew == "half":
+            logits[:, ::2] -= 60.0
+        ids, _, _ = oracle.route(logits, k)
+        offsets, _, _ = oracle.permute(ids, E)
+        R = T * k
+        a_gu = synth.normal_bf16((R, H), 1.0, 7, 100)
+        a_dn = synth.normal_bf16((R, I), 4.0, 7, 101)
+        ref_h = oracle.gateup_rows(a_gu, offsets, layer, range(R))
+        ref_y = oracle.down_rows(a_dn, offsets, layer, range(R))
+        _gemm_cache[key] = (layer, offsets, a_gu, a_dn, ref_h, ref_y)
+    return _gemm_cache[key]

@@ -7,18 +7,11 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close_h, assert_close_rms, bf16_dev_to_f32, dev
+from tests.gpu_util import GEMM_SHAPES, assert_close_h, assert_close_rms, bf16_dev_to_f32, dev, gemm_problem
 
 pytestmark = pytest.mark.gpu
 
-# (E, k, H, I, T, skew)
-SHAPES = [
-    (8, 2, 256, 128, 16, None),        # the tiny layer
-    (5, 3, 288, 96, 37, None),         # K tails: H % 256 != 0, I % 64 != 0
-    (3, 2, 512, 256, 200, None),       # several token chunks per expert
-    (1, 1, 1024, 512, 300, None),      # one expert owns every row
-    (16, 4, 2048, 1024, 64, "half"),   # deep K, empty experts
-]
+SHAPES = GEMM_SHAPES
 
 
 def impl_flags(B):
@@ -30,25 +23,7 @@ def impl_flags(B):
     }
 
 
-_cache = {}
-
-
-def problem(E, k, H, I, T, skew):
-    key = (E, k, H, I, T, skew)
-    if key not in _cache:
-        layer = synth.make_layer(synth.LayerShape(E=E, top_k=k, H=H, I=I), seed=E + H)
-        logits = np.random.default_rng(T).standard_normal((T, E)).astype(np.float32)
-        if skew == "half":
-            logits[:, ::2] -= 60.0
-        ids, _, _ = oracle.route(logits, k)
-        offsets, _, _ = oracle.permute(ids, E)
-        R = T * k
-        a_gu = synth.normal_bf16((R, H), 1.0, 7, 100)
-        a_dn = synth.normal_bf16((R, I), 4.0, 7, 101)
-        ref_h = oracle.gateup_rows(a_gu, offsets, layer, range(R))
-        ref_y = oracle.down_rows(a_dn, offsets, layer, range(R))
-        _cache[key] = (layer, offsets, a_gu, a_dn, ref_h, ref_y)
-    return _cache[key]
+problem = gemm_problem
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"E{s[0]}k{s[1]}H{s[2]}I{s[3]}T{s[4]}" for s in SHAPES])

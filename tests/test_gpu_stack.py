@@ -74,15 +74,37 @@ def test_stack_in_place(cuda_lib):
     assert np.array_equal(host(xd), want)
 
 
-def test_full_size_two_layer_stack_on_sampled_tokens(cuda_lib):
-    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Stack
-    T = 256
-    arrays, layers, stack, x, logits = make_stack(synth.FULL, 2, T)
-    tokens = np.sort(np.random.default_rng(0).choice(T, 6, replace=False))
-    chained = teacher_forced(arrays, layers, MoeW4A16Stack, x, logits, 8, tokens=tokens)
+@pytest.mark.slow
+def test_full_size_twelve_layer_stack_teacher_forced(cuda_lib):
+    """The benchmarked stack (12 full-size layers, T = 256; layer l's weights and logits seed l,
+    x seed 0): every layer against the oracle on its own seeded 16-token sample, fed the GPU's
+    input of that layer; then the whole stack in one call equals the chained calls bit for bit.
+    One layer's host arrays exist at a time."""
+    import os
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer, MoeW4A16Stack
+    shape, T, L = synth.FULL, 256, 12
+    x, _ = synth.make_tokens(T, shape.H, shape.E, seed=0)
+    layers, logits = [], []
+    cur = dev(x)
+    for l in range(L):
+        arrays = synth.make_layer(shape, seed=l)
+        lay = MoeW4A16Layer.from_arrays(shape, arrays)
+        lg = synth.make_tokens(T, shape.H, shape.E, seed=l)[1]
+        one = MoeW4A16Stack([lay])
+        nxt = one.forward(cur, [dev(lg)])
+        assert one.check_status() == 0
+        tokens = np.sort(np.random.default_rng(l).choice(T, 16, replace=False))
+        ref = oracle.stack_layer(host(cur, np.uint16), lg, arrays, shape.top_k, tokens=tokens,
+                                 workers=os.cpu_count() or 1)
+        assert_close_rms(bf16_dev_to_f32(nxt)[tokens], ref["out"], what=f"layer {l}")
+        del arrays, ref
+        layers.append(lay)
+        logits.append(lg)
+        cur = nxt
+    stack = MoeW4A16Stack(layers)
     whole = stack.forward(dev(x), [dev(v) for v in logits])
     assert stack.check_status() == 0
-    assert np.array_equal(host(whole), host(chained))
+    assert np.array_equal(host(whole), host(cur))
 
 
 def test_tiny_stack_with_shared_experts_teacher_forced(cuda_lib):

@@ -267,6 +267,69 @@ def test_single_expert_top1_equals_dense_brute_force():
         assert np.abs(got - ref).max() <= 1e-5 * rms + 1e-12
 
 
+def brute_owner(offsets, r):
+    """The expert owning expert-sorted row r, by a plain scan of the offsets."""
+    owner = None
+    for e in range(len(offsets) - 1):
+        if offsets[e] <= r < offsets[e + 1]:
+            assert owner is None
+            owner = e
+    assert owner is not None
+    return owner
+
+
+# Offsets with empty experts at the start, in the middle and at the end, and a
+# second set whose last expert owns rows; every row sits next to a boundary.
+ROW_OFFSETS = [[0, 0, 3, 3, 7, 8, 8], [0, 2, 2, 2, 5, 5, 6]]
+
+
+@pytest.mark.parametrize("offsets", ROW_OFFSETS)
+def test_gateup_rows_use_each_rows_own_expert(offsets):
+    import synth
+    E, H, I = len(offsets) - 1, 64, 32
+    layer = rand_layer(E, H, I, seed=31)
+    R = offsets[-1]
+    a_bits = synth.normal_bf16((R, H), 1.0, 5, 0)
+    rows = list(np.random.default_rng(1).permutation(R))          # any order of rows
+    got = oracle.gateup_rows(a_bits, np.array(offsets, dtype=np.int32), layer, rows)
+    for p, r in enumerate(rows):
+        e = brute_owner(offsets, r)
+        x = [bf16_bits_to_float(b) for b in a_bits[r]]
+        W13 = [brute_dequant_row(layer["w13"][e][n], layer["s13"][e][n]) for n in range(2 * I)]
+        gu = [sum(a * b for a, b in zip(row, x)) for row in W13]
+        ref = np.array([gu[i] / (1.0 + math.exp(-gu[i])) * gu[I + i] for i in range(I)])
+        assert np.abs(got[p] - ref).max() <= 1e-5 * np.sqrt(np.mean(ref ** 2)), (r, e)
+
+
+@pytest.mark.parametrize("offsets", ROW_OFFSETS)
+def test_down_rows_use_each_rows_own_expert(offsets):
+    import synth
+    E, H, I = len(offsets) - 1, 64, 32
+    layer = rand_layer(E, H, I, seed=32)
+    R = offsets[-1]
+    h_bits = synth.normal_bf16((R, I), 4.0, 6, 0)
+    rows = list(np.random.default_rng(2).permutation(R))
+    got = oracle.down_rows(h_bits, np.array(offsets, dtype=np.int32), layer, rows)
+    for p, r in enumerate(rows):
+        e = brute_owner(offsets, r)
+        h = [bf16_bits_to_float(b) for b in h_bits[r]]
+        W2 = [brute_dequant_row(layer["w2"][e][n], layer["s2"][e][n]) for n in range(H)]
+        ref = np.array([sum(a * b for a, b in zip(row, h)) for row in W2])
+        assert np.abs(got[p] - ref).max() <= 1e-5 * np.sqrt(np.mean(ref ** 2)), (r, e)
+
+
+def test_rows_of_neighbouring_experts_differ():
+    """The experts of the row pins are distinct, so a row read with its neighbour's expert fails them."""
+    E, H, I = 6, 64, 32
+    layer = rand_layer(E, H, I, seed=31)
+    import synth
+    a = synth.normal_bf16((1, H), 1.0, 5, 0)
+    outs = [oracle.gateup_rows(a, np.array([0] * e + [1] * (E + 1 - e), dtype=np.int32), layer, [0])[0]
+            for e in range(1, E + 1)]
+    for e in range(E - 1):
+        assert np.abs(outs[e] - outs[e + 1]).max() > 0.1 * np.sqrt(np.mean(outs[e] ** 2))
+
+
 def test_gate_and_up_are_not_interchangeable():
     """Swapping the gate and up halves changes the output (pins which half is the gate)."""
     layer = rand_layer(1, 64, 32, seed=2)

@@ -21,7 +21,7 @@
 // the gather writes x rows that way and the gate/up epilogue writes h that
 // way, at no extra cost.
 //
-// One persistent CTA per SM, 15 warps:
+// One persistent CTA per SM, 16 warps:
 //   warp 0      builds the tile list, then is the weight producer: TMA of int4
 //               words + bf16 scales (or dense bf16 weights) into the weight ring.
 //   warp 14     token-row producer: TMA of the token rows into their ring; a

@@ -7,7 +7,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
+#include "moe_w4a16.h"
+
 namespace moe {
+
+// Largest number of token-expert assignments (T * top_k) any entry point accepts.
+constexpr int64_t kMaxRows = int64_t(1) << 24;
+
+// The assignment-count rule shared by every entry point: MOE_OK, MOE_ERR_INVALID_ARG for T < 0,
+// or MOE_ERR_UNSUPPORTED_SHAPE beyond kMaxRows.
+inline moe_status_t check_T(int32_t T, int32_t k) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(T) * k > kMaxRows) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+// An NVTX range named after a C-ABI entry point, open for the call's host-side
+// life (argument checks and launches), so profilers attribute each kernel to
+// the call that launched it. Costs one pointer test when no tool is attached.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 // counts kernels launched by this library (moe_launch_count)
 void count_launches(uint64_t n);

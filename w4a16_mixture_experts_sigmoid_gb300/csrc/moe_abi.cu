@@ -22,7 +22,6 @@ namespace {
 using namespace moe;
 
 constexpr int kMaxDevices = 64;
-constexpr int64_t kMaxRows = int64_t(1) << 24;  // T * top_k
 constexpr int kMaxDim = 32768;                  // H, I, shared_I
 constexpr int kSplitMaxT = 256;                 // the shared expert splits K for T up to this
 constexpr int kMaxSplit = 8;                    // K slices at most
@@ -58,12 +57,6 @@ moe_status_t check_dims(const moe_dims_t& d) {
   if (d.E < 1 || d.E > 1024 || d.top_k < 1 || d.top_k > d.E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d.group != 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d.H < 32 || d.H % 32 || d.H > kMaxDim || d.I < 32 || d.I % 32 || d.I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
-  return MOE_OK;
-}
-
-moe_status_t check_T(int32_t T, int32_t k) {
-  if (T < 0) return MOE_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(T) * k > kMaxRows) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
@@ -323,6 +316,7 @@ size_t moe_host_staging_size(moe_dims_t d, int32_t T) {
 
 moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* topk_ids, float* topk_w,
                        void* stream) {
+  CallRange range_("moe_route");
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
@@ -334,6 +328,7 @@ moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int
 }
 
 moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream) {
+  CallRange range_("moe_sigmoid_scores");
   if (n < 0) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
   if (logits == nullptr || scores == nullptr) return MOE_ERR_INVALID_ARG;
@@ -346,6 +341,7 @@ moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, v
 moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t k, int32_t* expert_offsets,
                          int32_t* sorted_token_ids, int32_t* inv_perm, const uint16_t* x, int32_t H,
                          uint16_t* x_perm, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_permute");
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -375,6 +371,7 @@ moe_status_t moe_permute(const int32_t* topk_ids, int32_t T, int32_t E, int32_t 
 moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_t* w, const uint16_t* a_rows,
                                     int32_t T, const int32_t* expert_offsets, uint16_t* out_rows, void* ws,
                                     size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_w4a16_grouped_gemm");
   if (op != MOE_GEMM_GATEUP_SILU && op != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
@@ -398,6 +395,7 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
 
 moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* out,
                                void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_shared_expert");
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
@@ -419,6 +417,7 @@ moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint1
 
 moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w, int32_t T, int32_t k,
                          int32_t H, const uint16_t* addend, uint16_t* out, void* stream) {
+  CallRange range_("moe_combine");
   if (T < 0 || k < 1 || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
   if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
@@ -432,6 +431,7 @@ moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const 
 
 moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits, int32_t T,
                          uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_forward");
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
@@ -449,6 +449,7 @@ moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x
 moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host, const float* logits_host,
                               int32_t T, uint16_t* out_host, void* ws, size_t ws_bytes, uint32_t flags,
                               void* stream) {
+  CallRange range_("moe_forward_host");
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
@@ -483,6 +484,7 @@ moe_status_t moe_check_status(void* ws, void* stream) {
 }
 
 moe_status_t moe_rmsnorm(const uint16_t* x, int32_t T, int32_t H, float eps, uint16_t* out, void* stream) {
+  CallRange range_("moe_rmsnorm");
   if (T < 0 || H < 8 || H % 8 || H > kMaxDim || !(eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (x == nullptr || out == nullptr || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -501,6 +503,7 @@ size_t moe_stack_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint3
 moe_status_t moe_stack_forward(moe_dims_t d, const moe_weights_t* layers, int32_t L, const float* const* logits,
                                const uint16_t* x, int32_t T, float eps, uint16_t* out, void* ws, size_t ws_bytes,
                                uint32_t flags, void* stream) {
+  CallRange range_("moe_stack_forward");
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
@@ -539,6 +542,7 @@ moe_status_t moe_stack_forward(moe_dims_t d, const moe_weights_t* layers, int32_
 uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
 
 moe_status_t moe_debug_expire_wait(void* ws, int64_t timeout_ns, void* stream) {
+  CallRange range_("moe_debug_expire_wait");
   if (ws == nullptr) return MOE_ERR_INVALID_ARG;
   if (timeout_ns < 1000000) timeout_ns = 1000000;
   if (timeout_ns > 2000000000) timeout_ns = 2000000000;

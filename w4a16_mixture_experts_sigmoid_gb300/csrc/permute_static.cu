@@ -28,43 +28,53 @@ constexpr int kMaxScratchDevices = 64;
 // start at zero.
 static __device__ __align__(256) uint8_t g_permute_scratch[MOE_PERMUTE_STATIC_SCRATCH_BYTES];
 
+// Per-device set-up state. A successful lookup is kept for the life of the
+// process; so is the verdict that a device is not a compute capability 10.3
+// part, which cannot change. A lookup that failed for any other reason (for
+// example a first call made inside a stream capture, or an earlier error) is
+// not kept: the next call on that device tries again.
 struct ScratchSlot {
+  std::mutex mu;
   void* ptr = nullptr;
-  moe_status_t setup = MOE_ERR_CUDA;
+  bool unsupported = false;
 };
 
 ScratchSlot g_slot[kMaxScratchDevices];
-std::once_flag g_slot_once[kMaxScratchDevices];
 
-// Once per device, with that device current: check it is a compute capability
-// 10.3 part and look up the device address of the scratch array. The lookup
-// loads this library's module on the device if it is not loaded yet.
+// With the device current: check it is a compute capability 10.3 part and look
+// up the device address of the scratch array (this may load the library's
+// module onto the device).
 moe_status_t scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_CUDA;
-  std::call_once(g_slot_once[dev], [dev] {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-      g_slot[dev].setup = MOE_ERR_CUDA;
-      return;
-    }
-    if (major != 10 || minor != 3) {
-      g_slot[dev].setup = MOE_ERR_UNSUPPORTED_DEVICE;
-      return;
-    }
-    void* ptr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_permute_scratch);
-    if (e != cudaSuccess || ptr == nullptr) {
-      (void)cudaGetLastError();  // leave no sticky error behind for the caller's next call
-      g_slot[dev].setup = MOE_ERR_CUDA;
-      return;
-    }
-    g_slot[dev].ptr = ptr;
-    g_slot[dev].setup = MOE_OK;
-  });
-  *out = g_slot[dev].ptr;
-  return g_slot[dev].setup;
+  ScratchSlot& slot = g_slot[dev];
+  std::lock_guard<std::mutex> lock(slot.mu);
+  if (slot.ptr != nullptr) {
+    *out = slot.ptr;
+    return MOE_OK;
+  }
+  if (slot.unsupported) return MOE_ERR_UNSUPPORTED_DEVICE;
+  // an error the caller left pending stays as it was; only this lookup's own failure is cleared
+  const cudaError_t pending = cudaPeekAtLastError();
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    if (pending == cudaSuccess) (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) {
+    slot.unsupported = true;
+    return MOE_ERR_UNSUPPORTED_DEVICE;
+  }
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_permute_scratch);
+  if (e != cudaSuccess || ptr == nullptr) {
+    if (pending == cudaSuccess) (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  slot.ptr = ptr;
+  *out = ptr;
+  return MOE_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -79,10 +89,11 @@ moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, int32_t T, int3
                                         const uint16_t* x, int32_t H, uint16_t* x_perm, int32_t* status,
                                         uint32_t flags, void* stream) {
   using namespace moe;
+  CallRange range_("moe_permute_static_scratch");
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if (E < 1 || E > 1024 || k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;   // the same row limit as moe_permute
   const int64_t Tk = static_cast<int64_t>(T) * k;
-  if (Tk > (int64_t(1) << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T == 0) return MOE_OK;
   if (topk_ids == nullptr || expert_offsets == nullptr || sorted_token_ids == nullptr || inv_perm == nullptr)
     return MOE_ERR_INVALID_ARG;
