@@ -375,7 +375,7 @@ def run_ours(args):
     d_inv = torch.empty(R, dtype=torch.int32, device=dev)
     xperm = torch.empty((R, s.H), dtype=torch.int16, device=dev)
     h = torch.empty((R, s.I), dtype=torch.int16, device=dev)
-    y = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    y = torch.empty((R, s.H), dtype=torch.float32, device=dev)     # the layer keeps y in fp32
     wsp = layer.workspace(T)
     # the split calls chain as moe_forward runs them: rows in the tensor-core K order unless on the CUDA-core path
     order = 0 if (flags & B.MOE_FLAG_GEMM_SIMT) else B.MOE_FLAG_ROWS_MMA_ORDER
@@ -414,9 +414,15 @@ def run_ours(args):
         raise RuntimeError(f"device status after the timed region: {B.moe_status_string(st)}")
     value = whole_job_tokens_per_s(T, world, ms_max * 1e-3)
 
-    # per-kernel pass: the same kernels through the split entry points, events between them
+    # per-kernel pass: the same kernels through the split entry points, events between them (the
+    # shared expert, when the layer has one, as one entry: its two GEMMs and their K-slice finishes)
     ksteps = max(10, min(args.steps, 100))
-    names = ["route", "permute_gather", "gemm_gate_up", "gemm_down", "combine"]
+    names = ["route", "permute_gather", "gemm_gate_up", "gemm_down"]
+    ys = None
+    if s.shared_I:
+        names.append("shared_expert")
+        ys = torch.empty((T, s.H), dtype=torch.float32, device=dev)
+    names.append("combine")
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(ksteps)]
     for i in range(ksteps):
         E_ = ev[i]
@@ -428,10 +434,16 @@ def run_ours(args):
         B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp,
                                  flags | order)
         E_[3].record(stream)
-        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags | order)
+        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp,
+                                 flags | order | B.MOE_FLAG_OUT_F32)
         E_[4].record(stream)
-        B.moe_combine(y, d_inv, d_w, T, s.top_k, s.H, None, out)
-        E_[5].record(stream)
+        j = 5
+        if ys is not None:
+            B.moe_shared_expert(layer.dims, layer.weights, xd, T, ys, wsp, flags | B.MOE_FLAG_OUT_F32)
+            E_[j].record(stream)
+            j += 1
+        B.moe_combine_f32(y, d_inv, d_w, T, s.top_k, s.H, ys, out)
+        E_[j].record(stream)
     torch.cuda.synchronize(dev)
     per = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(ksteps)) for j, n in
            enumerate(names)}
@@ -441,8 +453,16 @@ def run_ours(args):
         "gemm_down": touched * dn_b + R * s.I * 2 + R * s.H * 2,
     }
     flops = {"gemm_gate_up": 2.0 * R * s.H * 2 * s.I, "gemm_down": 2.0 * R * s.I * s.H}
-    dominant = max(("gemm_gate_up", "gemm_down"), key=lambda n: per[n])
+    gemms = ["gemm_gate_up", "gemm_down"]
+    if s.shared_I:
+        # bf16 weights [2Is][H] and [H][Is], x in, the result out (the intermediate is not counted)
+        alg["shared_expert"] = 3 * s.H * s.shared_I * 2 + 2 * T * s.H * 2
+        flops["shared_expert"] = 6.0 * T * s.H * s.shared_I
+        gemms.append("shared_expert")
+    dominant = max(gemms, key=lambda n: per[n])
     hbm, bf16_burst, bf16_sus, src = load_peaks()
+    kernels_roofline = {n: round(kernel_roofline(n, alg[n], flops[n], per[n], None, hbm, bf16_sus, src)["frac"], 4)
+                        for n in gemms}
     roofline = kernel_roofline(dominant, alg[dominant], flops[dominant], per[dominant],
                                profile_traffic(dominant, args.workload), hbm, bf16_sus, src)
     step_bytes = touched * (gu_b + dn_b) + T * s.H * 2 * 2 + T * s.E * 4
@@ -454,7 +474,8 @@ def run_ours(args):
     step_roof = {"touched_experts": touched, "bytes": step_bytes, "flops": step_flops,
                  "hbm_gbs": step_bytes / (ms * 1e-3) / 1e9, "tflops": step_flops / (ms * 1e-3) / 1e12,
                  "roofline_ms": max(t_hbm, t_tc) * 1e3, "frac": max(t_hbm, t_tc) / (ms * 1e-3),
-                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "kernels_ms": per}
+                 "bound": "hbm" if t_hbm >= t_tc else "tensor", "kernels_ms": per,
+                 "kernels_frac": kernels_roofline}
 
     # end to end: host buffers in, host result out, copies inside the timed region
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
@@ -570,7 +591,7 @@ def run_stack(args):
     xn = torch.empty((T, s.H), dtype=torch.int16, device=dev)
     xperm = torch.empty((R, s.H), dtype=torch.int16, device=dev)
     h = torch.empty((R, s.I), dtype=torch.int16, device=dev)
-    y = torch.empty((R, s.H), dtype=torch.int16, device=dev)
+    y = torch.empty((R, s.H), dtype=torch.float32, device=dev)
     xa = xd.clone()
     xb = torch.empty_like(xa)
     wsp = layers[0].workspace(T)
@@ -595,9 +616,11 @@ def run_stack(args):
             B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, lay.dims, lay.weights, xperm, T, d_off, h, wsp,
                                      flags | order)
             E_[4].record(stream)
-            B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, lay.dims, lay.weights, h, T, d_off, y, wsp, flags | order)
+            B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, lay.dims, lay.weights, h, T, d_off, y, wsp,
+                                     flags | order | B.MOE_FLAG_OUT_F32)
             E_[5].record(stream)
-            B.moe_combine(y, d_inv, d_w, T, k, s.H, cur, nxt)   # the residual as the combine's addend
+            # timing only: the stack's combine also adds the bf16 residual (one T x H read more)
+            B.moe_combine_f32(y, d_inv, d_w, T, k, s.H, None, nxt)
             E_[6].record(stream)
             if r == 0:
                 torch.cuda.synchronize(dev)

@@ -106,6 +106,12 @@ typedef struct {
  * way, so the calls chain exactly as moe_forward runs them; without it every
  * row is in natural order. */
 #define MOE_FLAG_ROWS_MMA_ORDER 0x4u
+/* The down projection (moe_w4a16_grouped_gemm with MOE_GEMM_DOWN, and the
+ * shared expert) writes its rows in fp32 instead of bf16: out_rows / out are
+ * then float arrays of the same shape, to be summed by moe_combine_f32.
+ * moe_forward keeps these rows in fp32 internally: the layer output is then
+ * rounded to bf16 once, in the combine. Not valid with MOE_GEMM_GATEUP_SILU. */
+#define MOE_FLAG_OUT_F32 0x8u
 /* Bits 8..15: token rows per tile of the tensor-core GEMM: 16, 32, 64 or 128
  * (16 or 32 with MOE_FLAG_A_SMEM); 0 lets the library choose from T * top_k / E.
  * Any other value makes the GEMM calls return MOE_ERR_UNSUPPORTED_SHAPE. */
@@ -214,7 +220,7 @@ MOE_API moe_status_t moe_permute_static_scratch(const int32_t* topk_ids, int32_t
  *   op = MOE_GEMM_DOWN:        K = I, out_rows bf16 [R][H], out = bf16(W2_e a).
  * flags: MOE_FLAG_GEMM_SIMT, MOE_FLAG_A_SMEM, MOE_FLAG_TOKENS_PER_TILE(n),
  * MOE_FLAG_ROWS_MMA_ORDER (a_rows and, for gate/up, out_rows in the tensor-core
- * K order). ws: the status word in its first 256 bytes; the tensor-core path
+ * K order), MOE_FLAG_OUT_F32 (down only: out_rows is fp32 [R][H]). ws: the status word in its first 256 bytes; the tensor-core path
  * with natural-order rows also rewrites a_rows into the K order right after
  * it, so ws_bytes >= 256 + R*K*2 (rounded up to 256) unless
  * MOE_FLAG_ROWS_MMA_ORDER or MOE_FLAG_GEMM_SIMT is set. */
@@ -228,7 +234,8 @@ MOE_API moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_
  * share of the checkpoint, outside the INT4 bank).
  * out bf16 [T][H] = Wd (SiLU(Wg x) .* (Wu x)) for
  * x bf16 [T][H], fp32 accumulation. Needs w->shared_wgu, w->shared_wd, and
- * moe_workspace_size(d, T, w->shared_I, flags) bytes of workspace. */
+ * moe_workspace_size(d, T, w->shared_I, flags) bytes of workspace. With
+ * MOE_FLAG_OUT_F32, out is fp32 [T][H]. */
 MOE_API moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, int32_t T,
                                uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
@@ -242,6 +249,15 @@ MOE_API moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, con
 MOE_API moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const float* topk_w,
                          int32_t T, int32_t k, int32_t H, const uint16_t* addend,
                          uint16_t* out, void* stream);
+
+/* moe_combine over fp32 rows: y_rows fp32 [T*k][H] (the down projection with
+ * MOE_FLAG_OUT_F32), addend fp32 [T][H] or NULL; the same sum in rank order,
+ * rounded to bf16 once. This is the combine moe_forward runs: with no bf16
+ * rounding of the rows before the sum, the layer's largest outputs keep their
+ * error within the stated bound. */
+MOE_API moe_status_t moe_combine_f32(const float* y_rows, const int32_t* inv_perm, const float* topk_w,
+                             int32_t T, int32_t k, int32_t H, const float* addend,
+                             uint16_t* out, void* stream);
 
 /* The whole layer. Passage: "feat(pytorch): support Kimi K2.6", Motivation
  * and Changes (the compressed-tensors W4A16 MoE with its routing) and

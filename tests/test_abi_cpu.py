@@ -93,6 +93,8 @@ def test_arguments_rejected_before_any_launch(lib):
     assert L.moe_shared_expert(d, byref(w), 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(None, 16, 16, 4, 2, 256, None, 16, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(16, 16, 16, 4, 2, 250, None, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_f32(None, 16, 16, 4, 2, 256, None, 16, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_combine_f32(16, 16, 16, 4, 2, 250, None, 16, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_check_status(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_debug_expire_wait(None, 1000, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward_host(d, byref(w), None, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG

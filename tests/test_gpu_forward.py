@@ -112,6 +112,26 @@ def test_combine_alone_rounds_once(cuda_lib):
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.abs(ref).max())
 
 
+def test_combine_f32_rounds_once(cuda_lib):
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    rng = np.random.default_rng(4)
+    T, k, E, H = 61, 8, 40, 264
+    ids, w, _ = oracle.route(rng.standard_normal((T, E)).astype(np.float32), k)
+    _, _, inv = oracle.permute(ids, E)
+    y = (rng.standard_normal((T * k, H)) * 30).astype(np.float32)
+    add = rng.standard_normal((T, H)).astype(np.float32)
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    B.moe_combine_f32(dev(y), dev(inv), dev(w), T, k, H, dev(add), out)
+    ref = oracle.combine(y, inv, w, add)
+    got = bf16_dev_to_f32(out)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-6 * np.abs(ref).max())
+    out2 = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    B.moe_combine_f32(dev(y), dev(inv), dev(w), T, k, H, None, out2)
+    ref2 = oracle.combine(y, inv, w)
+    assert np.all(np.abs(bf16_dev_to_f32(out2) - ref2) <= 2.0 ** -8 * np.abs(ref2) + 1e-6 * np.abs(ref2).max())
+
+
 def test_forward_host_equals_forward_and_is_deterministic(cuda_lib):
     import torch
     from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer

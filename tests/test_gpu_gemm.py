@@ -66,7 +66,7 @@ def test_unsupported_tile_size_is_rejected(cuda_lib):
 
 @pytest.mark.parametrize("simt", [False, True])
 def test_split_calls_in_mma_order_chain_like_forward(cuda_lib, simt):
-    """route -> permute -> gate/up -> down -> combine with the tensor-core K order
+    """route -> permute -> gate/up -> down (fp32 rows) -> combine with the tensor-core K order
     for the exchanged rows gives exactly the bits of moe_forward."""
     import torch
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
@@ -87,14 +87,14 @@ def test_split_calls_in_mma_order_chain_like_forward(cuda_lib, simt):
     inv = torch.empty(R, dtype=torch.int32, device="cuda")
     xp = torch.empty((R, H), dtype=torch.int16, device="cuda")
     h = torch.empty((R, I), dtype=torch.int16, device="cuda")
-    y = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    y = torch.empty((R, H), dtype=torch.float32, device="cuda")     # the layer keeps y in fp32
     out = torch.empty((T, H), dtype=torch.int16, device="cuda")
     order = 0 if simt else B.MOE_FLAG_ROWS_MMA_ORDER
     B.moe_route(dev(logits), T, E, k, ids, w)
     B.moe_permute(ids, T, E, k, off, srt, inv, dev(x), H, xp, ws, order)
     B.moe_w4a16_grouped_gemm(0, layer.dims, layer.weights, xp, T, off, h, ws, flags | order)
-    B.moe_w4a16_grouped_gemm(1, layer.dims, layer.weights, h, T, off, y, ws, flags | order)
-    B.moe_combine(y, inv, w, T, k, H, None, out)
+    B.moe_w4a16_grouped_gemm(1, layer.dims, layer.weights, h, T, off, y, ws, flags | order | B.MOE_FLAG_OUT_F32)
+    B.moe_combine_f32(y, inv, w, T, k, H, None, out)
     assert B.moe_check_status(ws) == B.MOE_OK
     assert torch.equal(out, ref)
 
@@ -155,3 +155,29 @@ def test_small_and_large_experts_split_between_launches(cuda_lib):
     assert B.moe_check_status(ws) == B.MOE_OK
     assert_close_h(bf16_dev_to_f32(h), ref_h, what="gate/up split")
     assert_close_rms(bf16_dev_to_f32(y), ref_y, what="down split")
+
+
+@pytest.mark.parametrize("impl", ["tmem-auto", "simt"])
+def test_down_rows_in_fp32_are_the_unrounded_bf16_rows(cuda_lib, impl):
+    """MOE_FLAG_OUT_F32: the same down products, not rounded: rounding them to bf16 gives the
+    bf16 output bit for bit, and they match the oracle more closely than y's own bound."""
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    E, k, H, I, T, skew = SHAPES[2]
+    layer, offsets, a_gu, a_dn, ref_h, ref_y = problem(*SHAPES[2])
+    flags = impl_flags(B)[impl]
+    R = T * k
+    d = B.dims(E, k, H, I)
+    tens = {key: dev(v) for key, v in layer.items()}
+    w = B.weights(tens["w13"], tens["s13"], tens["w2"], tens["s2"])
+    ws = torch.zeros(B.moe_workspace_size(d, T), dtype=torch.uint8, device="cuda")
+    y16 = torch.empty((R, H), dtype=torch.int16, device="cuda")
+    y32 = torch.full((R, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.moe_w4a16_grouped_gemm(1, d, w, dev(a_dn), T, dev(offsets), y16, ws, flags)
+    B.moe_w4a16_grouped_gemm(1, d, w, dev(a_dn), T, dev(offsets), y32, ws, flags | B.MOE_FLAG_OUT_F32)
+    assert B.moe_check_status(ws) == B.MOE_OK
+    y32h = y32.cpu().numpy()
+    assert np.array_equal(oracle.f32_to_bf16(y32h), y16.cpu().numpy().view(np.uint16))
+    assert_close_rms(y32h, ref_y, what="down fp32")
+    with pytest.raises(B.MoeError):
+        B.moe_w4a16_grouped_gemm(0, d, w, dev(a_gu), T, dev(offsets), y32, ws, flags | B.MOE_FLAG_OUT_F32)

@@ -29,6 +29,7 @@ MOE_GEMM_DOWN = 1
 MOE_FLAG_GEMM_SIMT = 0x1
 MOE_FLAG_A_SMEM = 0x2
 MOE_FLAG_ROWS_MMA_ORDER = 0x4
+MOE_FLAG_OUT_F32 = 0x8
 MOE_PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -62,6 +63,8 @@ SIGNATURES = {
                                     c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_combine": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p,
                               c_void_p, c_void_p]),
+    "moe_combine_f32": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p,
+                                  c_void_p, c_void_p]),
     "moe_forward": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_void_p, c_int32, c_void_p,
                               c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_host_staging_size": (c_size_t, [moe_dims_t, c_int32]),
@@ -203,6 +206,11 @@ def moe_shared_expert(d: moe_dims_t, w: moe_weights_t, x, T: int, out, ws, flags
 def moe_combine(y_rows, inv_perm, topk_w, T: int, k: int, H: int, addend, out, stream=None) -> None:
     _check(load().moe_combine(_dptr(y_rows), _dptr(inv_perm), _dptr(topk_w), T, k, H, _dptr(addend), _dptr(out),
                               _stream(stream)), "moe_combine")
+
+
+def moe_combine_f32(y_rows, inv_perm, topk_w, T: int, k: int, H: int, addend, out, stream=None) -> None:
+    _check(load().moe_combine_f32(_dptr(y_rows), _dptr(inv_perm), _dptr(topk_w), T, k, H, _dptr(addend), _dptr(out),
+                                  _stream(stream)), "moe_combine_f32")
 
 
 def moe_forward(d: moe_dims_t, w: moe_weights_t, x, logits, T: int, out, ws, flags: int = 0, stream=None) -> None:

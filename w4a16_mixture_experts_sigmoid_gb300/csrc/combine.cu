@@ -1,5 +1,6 @@
 // Step 5: the top-k weighted combine back to token order,
 //   out[t] = bf16( sum_j w[t,j] * y[inv[t*k+j]]  (+ addend[t])  (+ residual[t]) ),
+// y and addend in bf16 or fp32 (the layer passes fp32: one bf16 rounding fewer),
 // fp32 accumulation in rank order j, then the shared expert's output, then the
 // residual stream of a layer stack, one rounding to bf16 at the end.
 // The pages' MoE sums the selected experts' outputs per token ("feat(pytorch):
@@ -25,10 +26,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
+// Eight consecutive values of a row: bf16 (one 16-byte load) or fp32 (two).
+template <bool F32>
+__device__ __forceinline__ void load8(const void* base, int64_t idx8, float (&f)[8]) {
+  if (F32) {
+    const float4* q = reinterpret_cast<const float4*>(base) + 2 * idx8;
+    const float4 a = __ldg(q), b = __ldg(q + 1);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  } else {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(base) + idx8), f);
+  }
+}
+
 // grid: (ceil(H/8 / blockDim), T); each thread owns 8 consecutive columns of one token.
-__global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ inv,
+template <bool F32>
+__global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y, const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k, int H8,
-                                                      const uint4* __restrict__ addend,
+                                                      const void* __restrict__ addend,
                                                       const uint4* __restrict__ residual, uint4* __restrict__ out) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H8) return;
@@ -41,7 +55,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
   for (int j0 = 0; j0 < k; j0 += 8) {
     int pj[8];
     float wj[8];
-    uint4 yv[8];
+    float yv[8][8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int j = j0 + u;
@@ -49,19 +63,19 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
       wj[u] = (j < k) ? __ldg(w + (int64_t)t * k + j) : 0.0f;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) yv[u] = (pj[u] >= 0) ? __ldg(y + (int64_t)pj[u] * H8 + c) : make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < 8; ++u) {
+      if (pj[u] >= 0) load8<F32>(y, (int64_t)pj[u] * H8 + c, yv[u]);
+    }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       if (pj[u] < 0) continue;
-      float f[8];
-      unpack8(yv[u], f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], f[i], acc[i]);
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], yv[u][i], acc[i]);
     }
   }
   if (addend != nullptr) {
     float f[8];
-    unpack8(__ldg(addend + (int64_t)t * H8 + c), f);
+    load8<F32>(addend, (int64_t)t * H8 + c, f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] += f[i];
   }
@@ -82,14 +96,17 @@ __global__ void __launch_bounds__(128) combine_kernel(const uint4* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
-                           const uint16_t* addend, const uint16_t* residual, uint16_t* out, cudaStream_t s) {
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int k, int H,
+                           const void* addend, const uint16_t* residual, bool y_f32, uint16_t* out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int H8 = H / 8;
   dim3 grid((H8 + 127) / 128, T < 65535 ? T : 65535);
-  combine_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const uint4*>(y), inv, w, T, k, H8,
-                                      reinterpret_cast<const uint4*>(addend), reinterpret_cast<const uint4*>(residual),
-                                      reinterpret_cast<uint4*>(out));
+  if (y_f32)
+    combine_kernel<true><<<grid, 128, 0, s>>>(y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
+                                              reinterpret_cast<uint4*>(out));
+  else
+    combine_kernel<false><<<grid, 128, 0, s>>>(y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
+                                               reinterpret_cast<uint4*>(out));
   count_launches(1);
   return cudaGetLastError();
 }

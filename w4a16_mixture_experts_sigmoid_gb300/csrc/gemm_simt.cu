@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_simt_kernel(GemmProblem p) {
         }
         int col = unit;
         if (OP == MOE_GEMM_GATEUP_SILU && p.out_mma_order) col = (unit & ~7) | ((unit & 3) << 1) | ((unit >> 2) & 1);
-        p.out[static_cast<int64_t>(t0 + t) * p.out_cols + col] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        const int64_t o = static_cast<int64_t>(t0 + t) * p.out_cols + col;
+        if (OP == MOE_GEMM_DOWN && p.out_f32 != nullptr) p.out_f32[o] = v;
+        else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
       }
     }
   }

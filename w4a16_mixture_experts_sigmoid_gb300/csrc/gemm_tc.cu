@@ -84,6 +84,7 @@ struct TcParams {
   const uint16_t* scales;
   const int32_t* offsets;
   uint16_t* out;
+  float* out_f32;          // down: fp32 rows instead of bf16 `out`, when set
   int* status;
   int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
   int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
@@ -639,9 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               const int row = ti.row0 + cb + c;
-              if (cb + c < ti.nvalid && row < p.R)
-                p.out[static_cast<int64_t>(row) * p.out_cols + n] =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
+              if (cb + c < ti.nvalid && row < p.R) {
+                const int64_t o = static_cast<int64_t>(row) * p.out_cols + n;
+                if (p.out_f32 != nullptr) p.out_f32[o] = __uint_as_float(v[c]);
+                else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
+              }
             }
           }
         }
@@ -716,7 +719,8 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
 // (gate/up: SiLU(gate) * up, as the epilogue computes it; down: the plain sum).
 template <int OP>
 __global__ void __launch_bounds__(256) splitk_finish_kernel(const float* __restrict__ part, int S, int R, int cols,
-                                                            int out_mma_order, uint16_t* __restrict__ out) {
+                                                            int out_mma_order, uint16_t* __restrict__ out,
+                                                            float* __restrict__ out_f32) {
   const int64_t n = static_cast<int64_t>(R) * cols;
   for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += static_cast<int64_t>(gridDim.x) * 256) {
     const int64_t row = i / cols;
@@ -732,7 +736,8 @@ __global__ void __launch_bounds__(256) splitk_finish_kernel(const float* __restr
     }
     const float v = (OP == MOE_GEMM_GATEUP_SILU) ? __fdividef(a, 1.0f + __expf(-a)) * b : a;
     const int oc = (OP == MOE_GEMM_GATEUP_SILU && out_mma_order) ? mma_order_pos(col) : col;
-    out[row * cols + oc] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    if (out_f32 != nullptr) out_f32[row * cols + oc] = v;
+    else out[row * cols + oc] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
 }
 
@@ -795,6 +800,7 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.scales = p.scales;
   prm.offsets = p.offsets;
   prm.out = p.out;
+  prm.out_f32 = (p.op == MOE_GEMM_DOWN) ? p.out_f32 : nullptr;
   prm.status = p.status;
   prm.E = p.E;
   prm.K = p.K;
@@ -824,9 +830,10 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   const int fb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   if (p.op == MOE_GEMM_GATEUP_SILU)
     splitk_finish_kernel<MOE_GEMM_GATEUP_SILU><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols,
-                                                                  p.out_mma_order ? 1 : 0, p.out);
+                                                                  p.out_mma_order ? 1 : 0, p.out, nullptr);
   else
-    splitk_finish_kernel<MOE_GEMM_DOWN><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols, 0, p.out);
+    splitk_finish_kernel<MOE_GEMM_DOWN><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols, 0, p.out,
+                                                           p.out_f32);
   count_launches(1);
   return cudaGetLastError();
 }

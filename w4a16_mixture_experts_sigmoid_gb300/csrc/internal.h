@@ -51,9 +51,9 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const in
 // dst = src rows (natural order) rewritten in MMA K order
 cudaError_t launch_to_mma_order(const uint16_t* src, uint16_t* dst, int64_t rows, int K, cudaStream_t s);
 
-// combine
-cudaError_t launch_combine(const uint16_t* y, const int32_t* inv, const float* w, int T, int k, int H,
-                           const uint16_t* addend, const uint16_t* residual, uint16_t* out, cudaStream_t s);
+// combine; y and addend are bf16 rows, or fp32 rows when y_f32 (the residual is always bf16)
+cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, int T, int k, int H,
+                           const void* addend, const uint16_t* residual, bool y_f32, uint16_t* out, cudaStream_t s);
 // out[t] = bf16(x[t] / sqrt(mean(x[t]^2) + eps)), fp32 arithmetic
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out, cudaStream_t s);
 
@@ -66,6 +66,7 @@ struct GemmProblem {
   const uint16_t* a;       // bf16 [R][K], expert-sorted rows
   const int32_t* offsets;  // [E+1], or null with uniform_rows >= 0
   uint16_t* out;           // bf16 [R][out_cols]
+  float* out_f32 = nullptr;  // down only: when set, the rows are written here in fp32 instead of `out`
   int* status;
   int E;
   int K;

@@ -99,9 +99,9 @@ Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
   L.hist = take(static_cast<size_t>(permute_blocks(static_cast<int64_t>(Tk))) * d.E * 4);
   L.xperm = take(Tk * d.H * 2);
   L.h = take(Tk * d.I * 2);
-  L.y = take(Tk * d.H * 2);
+  L.y = take(Tk * d.H * 4);   // fp32 rows: the down GEMM's output is not rounded before the combine
   L.hs = take(static_cast<size_t>(T) * shared_I * 2);
-  L.ys = take(shared_I > 0 ? static_cast<size_t>(T) * d.H * 2 : 0);
+  L.ys = take(shared_I > 0 ? static_cast<size_t>(T) * d.H * 4 : 0);
   // fp32 partial sums of the shared expert's K slices (small batches only)
   L.part_bytes = shared_I > 0 && T <= kSplitMaxT
                      ? static_cast<size_t>(kMaxSplit) * T * std::max(2 * shared_I, d.H) * 4 : 0;
@@ -134,15 +134,18 @@ int auto_tokens_per_tile(int64_t rows, int groups) {
 // One grouped GEMM. rows_mma_order: a (and, for gate/up, out) are stored in
 // the tensor-core K order. The tensor-core kernel needs its token rows in that
 // order; natural-order rows are first rewritten into `scratch` (R * K * 2 bytes).
+// out is bf16, or fp32 for the down projection with MOE_FLAG_OUT_F32.
 moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights_t* w, const uint16_t* a,
-                              int32_t T, const int32_t* offsets, uint16_t* out, int* status, uint32_t flags,
+                              int32_t T, const int32_t* offsets, void* out, int* status, uint32_t flags,
                               bool rows_mma_order, uint16_t* scratch, int sms, cudaStream_t s) {
   GemmProblem p;
   p.op = op;
   p.bf16_weights = false;
   p.a = a;
   p.offsets = offsets;
-  p.out = out;
+  const bool f32 = op == MOE_GEMM_DOWN && (flags & MOE_FLAG_OUT_F32);
+  p.out = f32 ? nullptr : static_cast<uint16_t*>(out);
+  p.out_f32 = f32 ? static_cast<float*>(out) : nullptr;
   p.status = status;
   p.E = d.E;
   p.R = T * d.top_k;
@@ -201,9 +204,9 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
 // The dense shared expert. Its weights make only 2*Is/128 gate/up and H/128 down tiles, fewer
 // than the SMs when a small batch fills one token tile; then each GEMM splits its K loop into
 // slices (fp32 partial sums in `part`, finished by a second kernel) so that every SM streams
-// weights. part may be null (no split).
+// weights. part may be null (no split). out is bf16, or fp32 with MOE_FLAG_OUT_F32.
 moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* hs,
-                        uint16_t* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
+                        void* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
   const int Is = w->shared_I;
   GemmProblem p;
   p.bf16_weights = true;
@@ -236,7 +239,9 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   p.op = MOE_GEMM_DOWN;
   p.w = w->shared_wd;
   p.a = hs;
-  p.out = out;
+  const bool f32 = (flags & MOE_FLAG_OUT_F32) != 0;
+  p.out = f32 ? nullptr : static_cast<uint16_t*>(out);
+  p.out_f32 = f32 ? static_cast<float*>(out) : nullptr;
   p.K = Is;
   p.rows_per_expert = d.H;
   p.out_cols = d.H;
@@ -260,7 +265,7 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
   int32_t* hist = reinterpret_cast<int32_t*>(ws + L.hist);
   uint16_t* xperm = reinterpret_cast<uint16_t*>(ws + L.xperm);
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
-  uint16_t* y = reinterpret_cast<uint16_t*>(ws + L.y);
+  float* y = reinterpret_cast<float*>(ws + L.y);
   const int R = T * d.top_k;
   // the tensor-core GEMMs exchange activation rows in their K order; the CUDA-core path in natural order
   const bool mma_order = (flags & MOE_FLAG_GEMM_SIMT) == 0;
@@ -271,18 +276,20 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
   moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, mma_order,
                                      nullptr, sms, s);
   if (st != MOE_OK) return st;
-  st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags, mma_order, nullptr, sms, s);
+  // y (and the shared expert's output) stay fp32 until the combine's one bf16 rounding
+  st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags | MOE_FLAG_OUT_F32, mma_order, nullptr,
+                        sms, s);
   if (st != MOE_OK) return st;
-  const uint16_t* addend = nullptr;
+  const float* addend = nullptr;
   if (w->shared_wgu != nullptr) {
     uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
-    uint16_t* ys = reinterpret_cast<uint16_t*>(ws + L.ys);
+    float* ys = reinterpret_cast<float*>(ws + L.ys);
     float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
-    st = run_shared(d, w, x, T, hs, ys, status, flags, sms, part, s);
+    st = run_shared(d, w, x, T, hs, ys, status, flags | MOE_FLAG_OUT_F32, sms, part, s);
     if (st != MOE_OK) return st;
     addend = ys;
   }
-  return cuda_status(launch_combine(y, inv, tw, T, d.top_k, d.H, addend, residual, out, s));
+  return cuda_status(launch_combine(y, inv, tw, T, d.top_k, d.H, addend, residual, true, out, s));
 }
 
 }  // namespace
@@ -373,6 +380,7 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
                                     size_t ws_bytes, uint32_t flags, void* stream) {
   CallRange range_("moe_w4a16_grouped_gemm");
   if (op != MOE_GEMM_GATEUP_SILU && op != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
+  if (op == MOE_GEMM_GATEUP_SILU && (flags & MOE_FLAG_OUT_F32)) return MOE_ERR_INVALID_ARG;
   moe_status_t st = check_dims(d);
   if (st != MOE_OK) return st;
   if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
@@ -389,7 +397,8 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, out_rows, reinterpret_cast<int*>(w8), flags, rows_mma,
+  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, static_cast<void*>(out_rows), reinterpret_cast<int*>(w8),
+                          flags, rows_mma,
                           convert ? reinterpret_cast<uint16_t*>(w8 + 256) : nullptr, di.sms, as_stream(stream));
 }
 
@@ -426,7 +435,21 @@ moe_status_t moe_combine(const uint16_t* y_rows, const int32_t* inv_perm, const 
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
-  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, nullptr, out, as_stream(stream)));
+  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, nullptr, false, out, as_stream(stream)));
+}
+
+moe_status_t moe_combine_f32(const float* y_rows, const int32_t* inv_perm, const float* topk_w, int32_t T, int32_t k,
+                             int32_t H, const float* addend, uint16_t* out, void* stream) {
+  CallRange range_("moe_combine_f32");
+  if (T < 0 || k < 1 || H < 8 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (check_T(T, k) != MOE_OK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (y_rows == nullptr || inv_perm == nullptr || topk_w == nullptr || out == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_rows) || !aligned16(out) || (addend != nullptr && !aligned16(addend))) return MOE_ERR_INVALID_ARG;
+  DevInfo di;
+  moe_status_t st = current_device(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_combine(y_rows, inv_perm, topk_w, T, k, H, addend, nullptr, true, out, as_stream(stream)));
 }
 
 moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits, int32_t T,
