@@ -112,6 +112,15 @@ typedef struct {
  * moe_forward keeps these rows in fp32 internally: the layer output is then
  * rounded to bf16 once, in the combine. Not valid with MOE_GEMM_GATEUP_SILU. */
 #define MOE_FLAG_OUT_F32 0x8u
+/* Run the int4 grouped GEMMs on CTA pairs: one tensor-core MMA (M = 256)
+ * covers the weight rows of two SMs, each SM dequantising its own 128 rows and
+ * loading half of the token rows. Same results as the one-SM kernel up to the
+ * order of fp32 additions inside the tensor cores. Ignored with
+ * MOE_FLAG_GEMM_SIMT or MOE_FLAG_A_SMEM. */
+#define MOE_FLAG_GEMM_PAIR 0x10u
+/* moe_workspace_size(..., MOE_FLAG_ROUTER_PROJECT) sizes the workspace of
+ * moe_forward_project (the layer plus the router's logits). */
+#define MOE_FLAG_ROUTER_PROJECT 0x20u
 /* Bits 8..15: token rows per tile of the tensor-core GEMM: 16, 32, 64 or 128
  * (16 or 32 with MOE_FLAG_A_SMEM); 0 lets the library choose from T * top_k / E.
  * Any other value makes the GEMM calls return MOE_ERR_UNSUPPORTED_SHAPE. */
@@ -141,6 +150,28 @@ MOE_API size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uin
  * weights are 1/k when that sum is 0. Bit-identical on every device. */
 MOE_API moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k,
                        int32_t* topk_ids, float* topk_w, void* stream);
+
+/* The router's logit projection. Passage: "feat(pytorch): support Kimi K2.6",
+ * Motivation and Changes ("MoE routing"); "Kimi-K2.6" catalog page, GEOMETRY
+ * (hidden 7168, 384 routed experts). The pages print no router; the reading
+ * is the plain linear gate of a routed MoE:
+ *   logits fp32 [T][E] = x bf16 [T][H] . w_gate^T, w_gate bf16 [E][H],
+ * products of bf16 values summed in fp32 on the tensor cores (the order of
+ * the fp32 additions is the hardware's: logits agree with an fp32 reference
+ * to rounding, not bit for bit). H a multiple of 32, 1 <= E <= 1024.
+ * ws: the status word in its first 256 bytes, then the K-slice sums of small
+ * batches; ws_bytes >= moe_router_workspace_size(T, E, H). flags:
+ * MOE_FLAG_GEMM_SIMT runs the CUDA-core kernel instead. */
+MOE_API size_t moe_router_workspace_size(int32_t T, int32_t E, int32_t H);
+MOE_API moe_status_t moe_router_logits(const uint16_t* x, const uint16_t* w_gate, int32_t T, int32_t E,
+                               int32_t H, float* logits, void* ws, size_t ws_bytes, uint32_t flags,
+                               void* stream);
+
+/* moe_router_logits, then moe_route on those logits: topk_ids, topk_w as
+ * moe_route gives them (the selection is bit-exact for the logits written). */
+MOE_API moe_status_t moe_route_project(const uint16_t* x, const uint16_t* w_gate, int32_t T, int32_t E,
+                               int32_t H, int32_t k, float* logits, int32_t* topk_ids, float* topk_w,
+                               void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /* The router's score function alone, element-wise: scores[i] = score(logits[i]). */
 MOE_API moe_status_t moe_sigmoid_scores(const float* logits, int64_t n, float* scores, void* stream);
@@ -270,6 +301,14 @@ MOE_API moe_status_t moe_combine_f32(const float* y_rows, const int32_t* inv_per
 MOE_API moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits,
                          int32_t T, uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags,
                          void* stream);
+
+/* The whole layer from the token activations alone: the router logits are
+ * projected from x with w_gate (bf16 [E][H], as moe_router_logits) into the
+ * workspace, then the layer runs as moe_forward on them.
+ * ws_bytes >= moe_workspace_size(d, T, w->shared_I, MOE_FLAG_ROUTER_PROJECT). */
+MOE_API moe_status_t moe_forward_project(moe_dims_t d, const moe_weights_t* w, const uint16_t* w_gate,
+                                 const uint16_t* x, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
+                                 uint32_t flags, void* stream);
 
 /* moe_forward from and to HOST buffers: copies x_host and logits_host into the
  * workspace, runs the layer, copies the result to out_host, all enqueued on

@@ -42,6 +42,7 @@ __all__ = [
     "unpack_int4", "pack_int4", "dequant", "silu", "expert_mlp",
     "shared_expert", "combine", "moe_layer", "gateup_rows", "down_rows",
     "rmsnorm", "stack_layer", "f32_to_bf16", "expert_int4_params", "EXP_CONSTANTS",
+    "router_logits", "route_projected",
 ]
 
 
@@ -156,6 +157,27 @@ def route(logits: np.ndarray, k: int):
     if zero.any():
         w[zero, :] = F32(1.0) / F32(k)
     return ids, w, s
+
+
+def router_logits(x_bits: np.ndarray, wg_bits: np.ndarray) -> np.ndarray:
+    """The router's logit projection: logits[t, e] = sum_i x[t, i] * Wg[e, i], fp32.
+
+    The pages name MoE routing ("feat(pytorch): support Kimi K2.6", Motivation
+    and Changes) over 384 experts of hidden 7168 ("Kimi-K2.6" catalog page,
+    GEOMETRY) but print no router; the reading taken is the plain linear gate of
+    a routed MoE: bf16 token activations x [T, H] and a bf16 gate matrix
+    Wg [E, H], products summed in fp32 (numpy's fp32 BLAS as the matmul).
+    """
+    x = bf16_to_f32(x_bits)
+    wg = bf16_to_f32(wg_bits)
+    return (x @ wg.T).astype(np.float32)
+
+
+def route_projected(x_bits: np.ndarray, wg_bits: np.ndarray, k: int):
+    """route() of the projected logits: (ids, weights, scores, logits)."""
+    logits = router_logits(x_bits, wg_bits)
+    ids, w, s = route(logits, k)
+    return ids, w, s, logits
 
 
 def permute(ids: np.ndarray, E: int):

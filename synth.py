@@ -35,7 +35,7 @@ import numpy as np
 _CHUNK = 1 << 22  # elements per independently seeded chunk
 
 # tensor ids: keep every tensor of a layer on its own stream
-TID_W13, TID_S13, TID_W2, TID_S2, TID_SH_GU, TID_SH_D, TID_X, TID_LOGITS = range(8)
+TID_W13, TID_S13, TID_W2, TID_S2, TID_SH_GU, TID_SH_D, TID_X, TID_LOGITS, TID_GATE = range(9)
 
 
 @dataclass(frozen=True)
@@ -134,6 +134,12 @@ def make_layer(shape: LayerShape, seed: int = 0, scale_lo: float = 0.005, scale_
         w["sh_gu"] = normal_bf16((2 * Is, H), shared_std, seed, TID_SH_GU)
         w["sh_d"] = normal_bf16((H, Is), shared_std, seed, TID_SH_D)
     return w
+
+
+def make_gate(E: int, H: int, seed: int = 0) -> np.ndarray:
+    """Router gate matrix, bf16 bits [E, H], N(0, 1/H): with N(0, 1) activations the projected
+    logits are about N(0, 1), the router logits of the decode workloads."""
+    return normal_bf16((E, H), float(1.0 / np.sqrt(H)), seed, TID_GATE)
 
 
 def make_tokens(T: int, H: int, E: int, seed: int = 0, bias: np.ndarray | None = None):

@@ -99,3 +99,53 @@ def gemm_problem(E, k, H, I, T, skew):
         ref_y = oracle.down_rows(a_dn, offsets, layer, range(R))
         _gemm_cache[key] = (layer, offsets, a_gu, a_dn, ref_h, ref_y)
     return _gemm_cache[key]
+
+
+# ---------------------------------------------------------------------------
+# the layer's intended arithmetic, emulated on the CPU
+# ---------------------------------------------------------------------------
+# The tensor-core path feeds bf16(q * s) weights and bf16 token rows, sums in
+# fp32, rounds h = SiLU(g) * u to bf16 (the down GEMM's operand), keeps y in
+# fp32 and rounds the layer output to bf16 once. On outputs of several RMS the
+# output's own half-ulp is already ~1.3% of RMS, and over a few hundred
+# thousand outputs this arithmetic itself reaches max|err| ~0.03 RMS. The
+# layer configs keep the stated 3e-2 bound (and pass it); the extra small test
+# shapes are held to max(3e-2, EMU_MARGIN x the emulated error of the same
+# case): the GPU may be no worse than the arithmetic it implements.
+EMU_MARGIN = 1.1
+
+
+def _bf(v):
+    import oracle
+    return oracle.bf16_to_f32(oracle.f32_to_bf16(np.asarray(v, dtype=np.float32))).astype(np.float64)
+
+
+def emulated_layer(x_bits, logits, layer, k, with_shared=False):
+    """fp64 emulation of the tensor-core layer (bf16 weights and h, fp32 y, bf16 output) -> [T, H]."""
+    import oracle
+    ids, w, _ = oracle.route(logits, k)
+    X = oracle.bf16_to_f32(x_bits).astype(np.float64)
+    T, H = X.shape
+    I = layer["w2"].shape[-1] * 8
+    out = np.zeros((T, H))
+    for e in np.unique(ids):
+        r, j = np.nonzero(ids == e)
+        W13 = _bf(oracle.dequant(layer["w13"][e], layer["s13"][e]))
+        W2 = _bf(oracle.dequant(layer["w2"][e], layer["s2"][e]))
+        gu = X[r] @ W13.T
+        h = _bf(gu[:, :I] / (1.0 + np.exp(-gu[:, :I])) * gu[:, I:])
+        out[r] += w[r, j].astype(np.float64)[:, None] * (h @ W2.T)
+    if with_shared:
+        Is = layer["sh_d"].shape[1]
+        gu = X @ oracle.bf16_to_f32(layer["sh_gu"]).astype(np.float64).T
+        h = _bf(gu[:, :Is] / (1.0 + np.exp(-gu[:, :Is])) * gu[:, Is:])
+        out += h @ oracle.bf16_to_f32(layer["sh_d"]).astype(np.float64).T
+    return _bf(out)
+
+
+def assert_close_layer(got, ref, x_bits, logits, layer, k, with_shared=False, what=""):
+    """The stated bound, or EMU_MARGIN x the emulated arithmetic's own max error if that is larger."""
+    emu = emulated_layer(x_bits, logits, layer, k, with_shared)
+    r = rms(ref)
+    emu_max = float(np.abs(emu - np.asarray(ref, dtype=np.float64)).max() / r) if r > 0 else 0.0
+    assert_close_rms(got, ref, max_rel=max(MAX_REL, EMU_MARGIN * emu_max), what=f"{what} (emulated {emu_max:.4f})")

@@ -95,6 +95,17 @@ def test_arguments_rejected_before_any_launch(lib):
     assert L.moe_combine(16, 16, 16, 4, 2, 250, None, 16, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine_f32(None, 16, 16, 4, 2, 256, None, 16, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine_f32(16, 16, 16, 4, 2, 250, None, 16, None) == B.MOE_ERR_INVALID_ARG
+    # router projection: shape rules and null pointers, before any launch
+    assert L.moe_router_logits(16, 16, 4, 384, 7000, 16, 16, 1 << 20, 0, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_router_logits(None, 16, 4, 384, 7168, 16, 16, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_logits(16, 16, 4, 384, 7168, None, 16, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_router_logits(16, 16, 4, 384, 7168, 16, 16, 16, 0, None) == B.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_router_logits(16, 16, 0, 384, 7168, 16, 16, 0, 0, None) == B.MOE_OK
+    assert L.moe_route_project(16, 16, 4, 384, 7168, 400, 16, 16, 16, 16, 1 << 20, 0, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_router_workspace_size(64, 384, 7168) > L.moe_router_workspace_size(512, 384, 7168) > 0
+    d2 = B.dims(384, 8, 7168, 2048)
+    assert L.moe_workspace_size(d2, 64, 0, B.MOE_FLAG_ROUTER_PROJECT) > L.moe_workspace_size(d2, 64, 0, 0)
     assert L.moe_check_status(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_debug_expire_wait(None, 1000, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward_host(d, byref(w), None, 16, 4, 16, 16, 1 << 30, 0, None) == B.MOE_ERR_INVALID_ARG

@@ -68,13 +68,13 @@ def test_decode_T64(full_layer):
     sampled_parity(arrays, layer, x, logits, np.arange(64))
 
 
-@pytest.mark.parametrize("variant", ["smem", "tokens32", "simt"])
+@pytest.mark.parametrize("variant", ["smem", "tokens32", "simt", "pair"])
 def test_decode_T64_other_paths(full_layer, variant):
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
     arrays, layer, _ = full_layer
     x, logits = synth.make_tokens(64, 7168, 384, seed=0)
     flags = {"smem": B.MOE_FLAG_A_SMEM, "tokens32": B.MOE_FLAG_TOKENS_PER_TILE(32),
-             "simt": B.MOE_FLAG_GEMM_SIMT}[variant]
+             "simt": B.MOE_FLAG_GEMM_SIMT, "pair": B.MOE_FLAG_GEMM_PAIR}[variant]
     sampled_parity(arrays, layer, x, logits, np.arange(0, 64, 8), flags=flags)
 
 

@@ -20,6 +20,9 @@ def impl_flags(B):
         "tmem-auto": 0, "tmem-16": T(16), "tmem-32": T(32), "tmem-64": T(64), "tmem-128": T(128),
         "smem-16": B.MOE_FLAG_A_SMEM | T(16), "smem-32": B.MOE_FLAG_A_SMEM | T(32),
         "simt": B.MOE_FLAG_GEMM_SIMT,
+        "pair-auto": B.MOE_FLAG_GEMM_PAIR, "pair-16": B.MOE_FLAG_GEMM_PAIR | T(16),
+        "pair-32": B.MOE_FLAG_GEMM_PAIR | T(32), "pair-64": B.MOE_FLAG_GEMM_PAIR | T(64),
+        "pair-128": B.MOE_FLAG_GEMM_PAIR | T(128),
     }
 
 
@@ -28,7 +31,7 @@ problem = gemm_problem
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"E{s[0]}k{s[1]}H{s[2]}I{s[3]}T{s[4]}" for s in SHAPES])
 @pytest.mark.parametrize("impl", ["tmem-auto", "tmem-16", "tmem-32", "tmem-64", "tmem-128", "smem-16", "smem-32",
-                                  "simt"])
+                                  "simt", "pair-auto", "pair-16", "pair-32", "pair-64", "pair-128"])
 def test_grouped_gemms_match_oracle(cuda_lib, shape, impl):
     import torch
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
@@ -127,7 +130,8 @@ def test_mma_order_rows_give_the_same_products(cuda_lib):
     assert torch.equal(dev(mma(h0.cpu().numpy())), h1)     # h comes back in the same K order
 
 
-def test_small_and_large_experts_split_between_launches(cuda_lib):
+@pytest.mark.parametrize("pair", [False, True])
+def test_small_and_large_experts_split_between_launches(cuda_lib, pair):
     """With many rows per expert on average the GEMMs run one launch with 32-token tiles for the
     experts with up to 32 rows and one with 128-token tiles for the rest: every row of both,
     including experts right at the boundary and an empty one, matches the oracle."""
@@ -150,8 +154,9 @@ def test_small_and_large_experts_split_between_launches(cuda_lib):
     off = dev(offsets)
     h = torch.full((R, I), 0x7FC0, dtype=torch.int16, device="cuda")
     y = torch.full((R, H), 0x7FC0, dtype=torch.int16, device="cuda")
-    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, d, w, dev(a_gu), T, off, h, ws, 0)
-    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(a_dn), T, off, y, ws, 0)
+    fl = B.MOE_FLAG_GEMM_PAIR if pair else 0
+    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, d, w, dev(a_gu), T, off, h, ws, fl)
+    B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(a_dn), T, off, y, ws, fl)
     assert B.moe_check_status(ws) == B.MOE_OK
     assert_close_h(bf16_dev_to_f32(h), ref_h, what="gate/up split")
     assert_close_rms(bf16_dev_to_f32(y), ref_y, what="down split")

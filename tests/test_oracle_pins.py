@@ -471,3 +471,50 @@ def test_stack_layer_single_expert_equals_brute_force():
         # fp32 against fp64 normalisation may put a few inputs one bf16 step apart
         assert np.abs(got - ref).max() <= 1e-2 * np.sqrt(np.mean(np.array(mlp) ** 2)) + 1e-6
         assert np.abs(got - ref).mean() <= 1e-4 * np.sqrt(np.mean(np.array(mlp) ** 2)) + 1e-6
+
+
+# ---------------------------------------------------------------------------
+# the router's logit projection
+# ---------------------------------------------------------------------------
+
+def test_router_logits_match_fp64_dot_products():
+    import synth
+    T, E, H = 5, 7, 96
+    x = synth.normal_bf16((T, H), 1.0, 3, 0)
+    wg = synth.normal_bf16((E, H), 0.05, 3, 1)
+    got = oracle.router_logits(x, wg)
+    for t in range(T):
+        xs = [bf16_bits_to_float(b) for b in x[t]]
+        for e in range(E):
+            ws = [bf16_bits_to_float(b) for b in wg[e]]
+            exact = sum(a * b for a, b in zip(xs, ws))
+            bound = H * 2.0 ** -24 * sum(abs(a * b) for a, b in zip(xs, ws))
+            assert abs(float(got[t, e]) - exact) <= bound, (t, e)
+
+
+def test_router_logits_scale_and_transpose():
+    """Doubling the gate doubles every logit exactly; row e of the gate makes column e."""
+    import synth
+    x = synth.normal_bf16((4, 64), 1.0, 4, 0)
+    wg = synth.normal_bf16((6, 64), 0.05, 4, 1)
+    a = oracle.router_logits(x, wg)
+    wg2 = oracle.f32_to_bf16(oracle.bf16_to_f32(wg) * 2)
+    assert np.array_equal(oracle.router_logits(x, wg2), a * 2)
+    one_hot = np.zeros((6, 64), dtype=np.uint16)
+    one_hot[2, 5] = 0x3F80                         # bf16 1.0: column 2 is x[:, 5]
+    b = oracle.router_logits(x, one_hot)
+    assert np.array_equal(b[:, 2], oracle.bf16_to_f32(x[:, 5]))
+    assert np.all(b[:, [0, 1, 3, 4, 5]] == 0)
+
+
+def test_identical_gate_rows_tie_to_the_lowest_expert():
+    import synth
+    x = synth.normal_bf16((8, 64), 1.0, 5, 0)
+    wg = synth.normal_bf16((10, 64), 0.05, 5, 1)
+    wg[7] = wg[2]                                   # experts 2 and 7 score the same for every token
+    ids, w, _, logits = oracle.route_projected(x, wg, 10)
+    assert np.array_equal(logits[:, 2], logits[:, 7])
+    for t in range(8):
+        pos = list(ids[t])
+        assert pos.index(2) < pos.index(7)
+        assert w[t, pos.index(2)] == w[t, pos.index(7)]

@@ -76,3 +76,18 @@ def test_emulation_reports(emulated, capsys):
     with capsys.disabled():
         for shape, ((hm, ha), (ym, ya)) in emulated.items():
             print(f"\n{shape}: h max {hm:.4f} mean {ha:.5f} RMS; y max {ym:.4f} mean {ya:.5f} RMS")
+
+
+def test_layer_emulation_tail_reaches_the_stated_bound():
+    """On a small layer whose expert 0 takes every one of 300 tokens, the intended arithmetic itself
+    lands at the stated 3e-2: the reason the extra test shapes compare against it."""
+    import synth
+    from tests.gpu_util import MAX_REL, emulated_layer, rms
+    E, k, H, I, T = 8, 2, 256, 128, 300
+    arrays = synth.make_layer(synth.LayerShape(E=E, top_k=k, H=H, I=I), seed=E + T)
+    x, logits = synth.make_tokens(T, H, E, seed=E + T + 1)
+    logits[:, 0] += 40.0
+    ref = oracle.moe_layer(x, logits, arrays, k)["out"].astype(np.float64)
+    emu = emulated_layer(x, logits, arrays, k)
+    worst = np.abs(emu - ref).max() / rms(ref)
+    assert 0.8 * MAX_REL < worst < 1.5 * MAX_REL, worst

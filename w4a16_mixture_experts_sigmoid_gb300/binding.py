@@ -30,6 +30,8 @@ MOE_FLAG_GEMM_SIMT = 0x1
 MOE_FLAG_A_SMEM = 0x2
 MOE_FLAG_ROWS_MMA_ORDER = 0x4
 MOE_FLAG_OUT_F32 = 0x8
+MOE_FLAG_GEMM_PAIR = 0x10
+MOE_FLAG_ROUTER_PROJECT = 0x20
 MOE_PERMUTE_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -53,6 +55,13 @@ SIGNATURES = {
     "moe_workspace_size": (c_size_t, [moe_dims_t, c_int32, c_int32, c_uint32]),
     "moe_route": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "moe_sigmoid_scores": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "moe_router_workspace_size": (c_size_t, [c_int32, c_int32, c_int32]),
+    "moe_router_logits": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_size_t,
+                                    c_uint32, c_void_p]),
+    "moe_route_project": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_forward_project": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_void_p, c_int32, c_void_p,
+                                      c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                               c_void_p, c_int32, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_permute_static_scratch": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
@@ -170,6 +179,28 @@ def moe_host_staging_size(d: moe_dims_t, T: int) -> int:
 
 def moe_route(logits, T: int, E: int, k: int, topk_ids, topk_w, stream=None) -> None:
     _check(load().moe_route(_dptr(logits), T, E, k, _dptr(topk_ids), _dptr(topk_w), _stream(stream)), "moe_route")
+
+
+def moe_router_workspace_size(T: int, E: int, H: int) -> int:
+    return int(load().moe_router_workspace_size(T, E, H))
+
+
+def moe_router_logits(x, w_gate, T: int, E: int, H: int, logits, ws, flags: int = 0, stream=None) -> None:
+    _check(load().moe_router_logits(_dptr(x), _dptr(w_gate), T, E, H, _dptr(logits), _dptr(ws), _nbytes(ws), flags,
+                                    _stream(stream)), "moe_router_logits")
+
+
+def moe_route_project(x, w_gate, T: int, E: int, H: int, k: int, logits, topk_ids, topk_w, ws, flags: int = 0,
+                      stream=None) -> None:
+    _check(load().moe_route_project(_dptr(x), _dptr(w_gate), T, E, H, k, _dptr(logits), _dptr(topk_ids),
+                                    _dptr(topk_w), _dptr(ws), _nbytes(ws), flags, _stream(stream)),
+           "moe_route_project")
+
+
+def moe_forward_project(d: moe_dims_t, w: moe_weights_t, w_gate, x, T: int, out, ws, flags: int = 0,
+                        stream=None) -> None:
+    _check(load().moe_forward_project(d, ctypes.byref(w), _dptr(w_gate), _dptr(x), T, _dptr(out), _dptr(ws),
+                                      _nbytes(ws), flags, _stream(stream)), "moe_forward_project")
 
 
 def moe_sigmoid_scores(logits, n: int, scores, stream=None) -> None:

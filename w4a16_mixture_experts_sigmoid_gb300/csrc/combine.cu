@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y
                                                       const float* __restrict__ w, int T, int k, int H8,
                                                       const void* __restrict__ addend,
                                                       const uint4* __restrict__ residual, uint4* __restrict__ out) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= H8) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
@@ -102,10 +104,10 @@ cudaError_t launch_combine(const void* y, const int32_t* inv, const float* w, in
   const int H8 = H / 8;
   dim3 grid((H8 + 127) / 128, T < 65535 ? T : 65535);
   if (y_f32)
-    combine_kernel<true><<<grid, 128, 0, s>>>(y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
+    (void)launch_pdl(combine_kernel<true>, dim3(grid), dim3(128), 0, s, y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
                                               reinterpret_cast<uint4*>(out));
   else
-    combine_kernel<false><<<grid, 128, 0, s>>>(y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
+    (void)launch_pdl(combine_kernel<false>, dim3(grid), dim3(128), 0, s, y, inv, w, T, k, H8, addend, reinterpret_cast<const uint4*>(residual),
                                                reinterpret_cast<uint4*>(out));
   count_launches(1);
   return cudaGetLastError();

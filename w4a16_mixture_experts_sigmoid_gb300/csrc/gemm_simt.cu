@@ -36,6 +36,8 @@ __device__ __forceinline__ void load_w8(const GemmProblem& p, int64_t row, int c
 
 template <int OP, bool BF16W>
 __global__ void __launch_bounds__(kWarps * 32) gemm_simt_kernel(GemmProblem p) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kWarps + warp;
   const int e = blockIdx.y;
@@ -112,11 +114,11 @@ cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t s) {
   const int groups = p.uniform_rows >= 0 ? 1 : p.E;
   dim3 grid((units + kWarps - 1) / kWarps, groups);
   if (p.op == MOE_GEMM_GATEUP_SILU) {
-    if (p.bf16_weights) gemm_simt_kernel<MOE_GEMM_GATEUP_SILU, true><<<grid, kWarps * 32, 0, s>>>(p);
-    else gemm_simt_kernel<MOE_GEMM_GATEUP_SILU, false><<<grid, kWarps * 32, 0, s>>>(p);
+    if (p.bf16_weights) (void)launch_pdl(gemm_simt_kernel<MOE_GEMM_GATEUP_SILU, true>, dim3(grid), dim3(kWarps * 32), 0, s, p);
+    else (void)launch_pdl(gemm_simt_kernel<MOE_GEMM_GATEUP_SILU, false>, dim3(grid), dim3(kWarps * 32), 0, s, p);
   } else {
-    if (p.bf16_weights) gemm_simt_kernel<MOE_GEMM_DOWN, true><<<grid, kWarps * 32, 0, s>>>(p);
-    else gemm_simt_kernel<MOE_GEMM_DOWN, false><<<grid, kWarps * 32, 0, s>>>(p);
+    if (p.bf16_weights) (void)launch_pdl(gemm_simt_kernel<MOE_GEMM_DOWN, true>, dim3(grid), dim3(kWarps * 32), 0, s, p);
+    else (void)launch_pdl(gemm_simt_kernel<MOE_GEMM_DOWN, false>, dim3(grid), dim3(kWarps * 32), 0, s, p);
   }
   count_launches(1);
   return cudaGetLastError();

@@ -53,8 +53,7 @@
 // MOE_ERR_DEVICE_TIMEOUT in the status word, every role leaves its loop, the
 // producer lets its copies in flight land, the MMA issuer lets its MMAs
 // finish, and the CTA frees its tensor memory before returning.
-#include "common.cuh"
-#include "internal.h"
+#include "gemm_tc_parts.cuh"
 
 #include <atomic>
 #include <cstring>
@@ -63,41 +62,8 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128;            // weight rows per tile (MMA M)
-constexpr int BK = 256;            // K per pipeline stage
-constexpr int KSUB = 64;           // K per 128-byte swizzle row
-constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
-constexpr int kThreads = 512;      // 16 warps, 128 registers a thread
-constexpr int kFirstDqWarp = 2;
-constexpr int kFirstEpiWarp = 10;
-constexpr int kBProducerWarp = 14;
-constexpr int kSecondMmaWarp = 15;
-constexpr int kMaxE = 1024;
-constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_100-class parts
-constexpr int kAlignSlack = 1024;
-constexpr int kAuxBytes = 7168;
+using namespace tc;
 
-struct TcParams {
-  CUtensorMap tm_w;  // int4 words [rows_total][K/8] (box 32 x 64) or bf16 weights [rows_total][K] (box 64 x 16)
-  CUtensorMap tm_s;  // bf16 scales [rows_total][K/32] (box 8 x 64), when scale_tma
-  CUtensorMap tm_b;  // bf16 token rows [R][K] (box 64 x NT)
-  const uint16_t* scales;
-  const int32_t* offsets;
-  uint16_t* out;
-  float* out_f32;          // down: fp32 rows instead of bf16 `out`, when set
-  int* status;
-  int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
-  int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
-  int ksplit;              // K slices per tile (1: whole K); > 1 (bf16 weights only) writes fp32 partial sums
-  float* partial;          // [ksplit][R][2][I] (gate/up) or [ksplit][R][H] (down), when ksplit > 1
-  unsigned long long timeout_ns;
-};
-
-// Shared memory holds two rings. The weight ring (int4 words + scales, or
-// dense bf16 weights) is released by the dequant warps as soon as they have
-// the stage in registers, so HBM streaming never waits on the tensor pipe; the
-// token-row ring (operand B) is released by the MMA commit. With dense bf16
-// weights the MMA reads both, and the two rings advance in lock step.
 template <int ASRC, int NT>
 struct Cfg {
   static constexpr bool kDq = ASRC != A_SMEM_BF16;
@@ -142,83 +108,6 @@ struct Cfg {
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-struct TileInfo {
-  int wt;      // weight tile (128 rows; for gate/up 64 gate + 64 up rows)
-  int e;       // expert
-  int row0;    // first token row of the chunk
-  int nvalid;  // token rows of the chunk that belong to the expert
-  int split;   // K slice: stages [split * nk, (split + 1) * nk) of the whole K loop
-};
-
-__device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t* act_e, const int* tpre,
-                                                const TcParams& p, int nt, int ksplit) {
-  int lo = 0, hi = n_act - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tpre[mid] <= i) lo = mid;
-    else hi = mid - 1;
-  }
-  TileInfo t;
-  t.e = act_e[lo];
-  int start, cnt;
-  if (p.uniform_rows >= 0) { start = 0; cnt = p.uniform_rows; }
-  else { start = p.offsets[t.e]; cnt = p.offsets[t.e + 1] - start; }
-  const int nch = (cnt + nt - 1) / nt;
-  int rem = i - tpre[lo];
-  t.split = 0;
-  if (ksplit > 1) {
-    t.split = rem % ksplit;
-    rem /= ksplit;
-  }
-  t.wt = rem / nch;
-  const int c = rem - t.wt * nch;
-  t.row0 = start + c * nt;
-  t.nvalid = min(nt, cnt - c * nt);
-  return t;
-}
-
-// Bounded wait by every lane of a warp, with a warp-uniform verdict: lanes that
-// saw the phase complete and lanes that timed out or saw the abort flag agree
-// on one outcome, so no .sync.aligned instruction runs with part of the warp.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const TcParams& p, volatile int* abort_flag) {
-  const bool ok = mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status);
-  return __all_sync(0xFFFFFFFFu, ok);
-}
-
-// One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
-// 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
-// 8i+m (low half) and 8i+m+4 (high half) of the chunk. Per pair of weights:
-// one lop3 makes the bf16 pattern 0x43<nibble> = 128 + nibble exactly, one
-// packed subtract of 136 gives q = nibble - 8 exactly, one packed multiply
-// rounds q*s once to nearest even. Written as PTX: the same two packed bf16
-// operations through the cuda_bf16 intrinsics take more issue slots.
-__device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bits, uint32_t* out16) {
-  const uint32_t s2 = (scale_bits & 0xFFFFu) * 0x10001u;  // the scale in both halves
-  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      uint32_t pr, q;
-      asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(pr) : "r"(w4[i] >> (4 * m)), "r"(0x000F000Fu), "r"(0x43004300u));
-      asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(pr), "r"(0x43084308u));   // 0x4308 = bf16 136
-      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(q), "r"(s2));
-    }
-  }
-}
-
-// A buffer b is reused every NB stages and the stages alternate between two dequant groups, so
-// its barriers are kept per (g % 2, b); the stages sharing one are P = lcm(2, NB) apart and g / P
-// counts the earlier ones. Buffer b is handed from stage g to stage g + NB: stage g waits for as
-// many releases of its (group, buffer) pair as there are stages g' <= g in its class mod P with
-// g' >= NB.
-__device__ __forceinline__ int a_releases_needed(int g, int nb, int period) {
-  return g / period + (g % period >= nb ? 1 : 0);
-}
-
-// position of input j inside its block of 8 when a row is stored in MMA order
-__device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1); }
-
 template <int OP, int ASRC, int NT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<ASRC, NT>;
@@ -245,6 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   int16_t* act_e = reinterpret_cast<int16_t*>(tmem_slot + 4);
   int* tpre = reinterpret_cast<int*>(act_e + kMaxE);
 
+  // The successor in the stream may launch now: its CTAs take SMs as this grid's CTAs leave, and
+  // only its token-row producer waits for this grid to finish (griddep_wait below). The tile
+  // table and the weight stream read nothing the predecessor writes: the expert offsets come
+  // from the permutation, which finished before the predecessor could start.
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = (OP == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
   // K slices exist only for the dense bf16 weights (the shared expert); the int4 kernels are
@@ -392,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == kBProducerWarp) {
     // ------------------------------------------------------------ token-row producer (one lane)
     if (lane == 0) {
+      griddep_wait();   // the token rows are the predecessor's output
       const uint64_t pol_b = l2_policy_evict_last();
       constexpr uint32_t txb = NSUB * NT * 128;
       int g = 0;
@@ -665,36 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 // host side
 // ---------------------------------------------------------------------------
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(ptr);
-  });
-  return fn;
-}
-
-bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
-                 uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
-  EncodeFn enc = get_encode();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[2] = {dim0, dim1};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int OP, int ASRC, int NT>
 cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
   using C = Cfg<ASRC, NT>;
@@ -710,7 +575,7 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  tc_gemm_kernel<OP, ASRC, NT><<<grid, kThreads, C::kSmemBytes, s>>>(prm);
+  (void)launch_pdl(tc_gemm_kernel<OP, ASRC, NT>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, prm);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -721,6 +586,8 @@ template <int OP>
 __global__ void __launch_bounds__(256) splitk_finish_kernel(const float* __restrict__ part, int S, int R, int cols,
                                                             int out_mma_order, uint16_t* __restrict__ out,
                                                             float* __restrict__ out_f32) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   const int64_t n = static_cast<int64_t>(R) * cols;
   for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += static_cast<int64_t>(gridDim.x) * 256) {
     const int64_t row = i / cols;
@@ -829,10 +696,10 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   const int64_t n = static_cast<int64_t>(p.R) * p.out_cols;
   const int fb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
   if (p.op == MOE_GEMM_GATEUP_SILU)
-    splitk_finish_kernel<MOE_GEMM_GATEUP_SILU><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols,
+    (void)launch_pdl(splitk_finish_kernel<MOE_GEMM_GATEUP_SILU>, dim3(fb), dim3(256), 0, s, p.partial, p.ksplit, p.R, p.out_cols,
                                                                   p.out_mma_order ? 1 : 0, p.out, nullptr);
   else
-    splitk_finish_kernel<MOE_GEMM_DOWN><<<fb, 256, 0, s>>>(p.partial, p.ksplit, p.R, p.out_cols, 0, p.out,
+    (void)launch_pdl(splitk_finish_kernel<MOE_GEMM_DOWN>, dim3(fb), dim3(256), 0, s, p.partial, p.ksplit, p.R, p.out_cols, 0, p.out,
                                                            p.out_f32);
   count_launches(1);
   return cudaGetLastError();

@@ -1,0 +1,163 @@
+// Pieces shared by the two tensor-core grouped-GEMM kernels (one CTA per tile in
+// gemm_tc.cu; a CTA pair per tile in gemm_pair.cu): the kernel parameters, the
+// tile decode of the persistent schedule, the int4 -> bf16 dequantisation, the
+// barrier arithmetic of the A buffers, and the host-side tensor-map encoding.
+// Included by those two translation units only.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+#include <mutex>
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;            // weight rows per tile (MMA M)
+constexpr int BK = 256;            // K per pipeline stage
+constexpr int KSUB = 64;           // K per 128-byte swizzle row
+constexpr int NSUB = BK / KSUB;    // swizzle sub-tiles per stage
+constexpr int kThreads = 512;      // 16 warps, 128 registers a thread
+constexpr int kFirstDqWarp = 2;
+constexpr int kFirstEpiWarp = 10;
+constexpr int kBProducerWarp = 14;
+constexpr int kSecondMmaWarp = 15;
+constexpr int kMaxE = 1024;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory per CTA on sm_100-class parts
+constexpr int kAlignSlack = 1024;
+constexpr int kAuxBytes = 7168;
+
+struct TcParams {
+  CUtensorMap tm_w;  // int4 words [rows_total][K/8] (box 32 x 64) or bf16 weights [rows_total][K] (box 64 x 16)
+  CUtensorMap tm_s;  // bf16 scales [rows_total][K/32] (box 8 x 64), when scale_tma
+  CUtensorMap tm_b;  // bf16 token rows [R][K] (box 64 x NT)
+  const uint16_t* scales;
+  const int32_t* offsets;
+  uint16_t* out;
+  float* out_f32;          // down: fp32 rows instead of bf16 `out`, when set
+  int* status;
+  int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
+  int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
+  int ksplit;              // K slices per tile (1: whole K); > 1 (bf16 weights only) writes fp32 partial sums
+  float* partial;          // [ksplit][R][2][I] (gate/up) or [ksplit][R][H] (down), when ksplit > 1
+  unsigned long long timeout_ns;
+};
+
+// Shared memory holds two rings. The weight ring (int4 words + scales, or
+// dense bf16 weights) is released by the dequant warps as soon as they have
+// the stage in registers, so HBM streaming never waits on the tensor pipe; the
+// token-row ring (operand B) is released by the MMA commit. With dense bf16
+// weights the MMA reads both, and the two rings advance in lock step.
+struct TileInfo {
+  int wt;      // weight tile (128 rows; for gate/up 64 gate + 64 up rows)
+  int e;       // expert
+  int row0;    // first token row of the chunk
+  int nvalid;  // token rows of the chunk that belong to the expert
+  int split;   // K slice: stages [split * nk, (split + 1) * nk) of the whole K loop
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int i, int n_act, const int16_t* act_e, const int* tpre,
+                                                const TcParams& p, int nt, int ksplit) {
+  int lo = 0, hi = n_act - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tpre[mid] <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  TileInfo t;
+  t.e = act_e[lo];
+  int start, cnt;
+  if (p.uniform_rows >= 0) { start = 0; cnt = p.uniform_rows; }
+  else { start = p.offsets[t.e]; cnt = p.offsets[t.e + 1] - start; }
+  const int nch = (cnt + nt - 1) / nt;
+  int rem = i - tpre[lo];
+  t.split = 0;
+  if (ksplit > 1) {
+    t.split = rem % ksplit;
+    rem /= ksplit;
+  }
+  t.wt = rem / nch;
+  const int c = rem - t.wt * nch;
+  t.row0 = start + c * nt;
+  t.nvalid = min(nt, cnt - c * nt);
+  return t;
+}
+
+// Bounded wait by every lane of a warp, with a warp-uniform verdict: lanes that
+// saw the phase complete and lanes that timed out or saw the abort flag agree
+// on one outcome, so no .sync.aligned instruction runs with part of the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const TcParams& p, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
+// 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
+// 8i+m (low half) and 8i+m+4 (high half) of the chunk. Per pair of weights:
+// one lop3 makes the bf16 pattern 0x43<nibble> = 128 + nibble exactly, one
+// packed subtract of 136 gives q = nibble - 8 exactly, one packed multiply
+// rounds q*s once to nearest even. Written as PTX: the same two packed bf16
+// operations through the cuda_bf16 intrinsics take more issue slots.
+__device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bits, uint32_t* out16) {
+  const uint32_t s2 = (scale_bits & 0xFFFFu) * 0x10001u;  // the scale in both halves
+  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      uint32_t pr, q;
+      asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(pr) : "r"(w4[i] >> (4 * m)), "r"(0x000F000Fu), "r"(0x43004300u));
+      asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(pr), "r"(0x43084308u));   // 0x4308 = bf16 136
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(q), "r"(s2));
+    }
+  }
+}
+
+// A buffer b is reused every NB stages and the stages alternate between two dequant groups, so
+// its barriers are kept per (g % 2, b); the stages sharing one are P = lcm(2, NB) apart and g / P
+// counts the earlier ones. Buffer b is handed from stage g to stage g + NB: stage g waits for as
+// many releases of its (group, buffer) pair as there are stages g' <= g in its class mod P with
+// g' >= NB.
+__device__ __forceinline__ int a_releases_needed(int g, int nb, int period) {
+  return g / period + (g % period >= nb ? 1 : 0);
+}
+
+// position of input j inside its block of 8 when a row is stored in MMA order
+__device__ __forceinline__ int mma_order_pos(int j) { return (j & ~7) | ((j & 3) << 1) | ((j >> 2) & 1); }
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(ptr);
+  });
+  return fn;
+}
+
+inline bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+                 uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+  EncodeFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+}  // namespace moe

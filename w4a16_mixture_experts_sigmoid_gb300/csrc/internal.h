@@ -88,6 +88,10 @@ enum ASource { A_TMEM_DQ = 0, A_SMEM_DQ = 1, A_SMEM_BF16 = 2 };
 // returns cudaErrorNotSupported if no kernel exists for (asrc, tokens_per_tile)
 cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int tokens_per_tile, int num_sms, cudaStream_t s);
 
+// the same GEMM on CTA pairs (int4 weights, A in tensor memory, rows in MMA K order): one
+// cta_group::2 MMA covers 256 weight rows over two SMs; nt in {16, 32, 64, 128}
+cudaError_t launch_gemm_pair(const GemmProblem& p, int tokens_per_tile, int num_sms, cudaStream_t s);
+
 cudaError_t launch_expire_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 
 }  // namespace moe

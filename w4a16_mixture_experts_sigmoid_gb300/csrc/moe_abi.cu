@@ -77,12 +77,18 @@ moe_status_t check_weights(const moe_weights_t* w, bool need_shared) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// Workspace layout of moe_forward (byte offsets, each 256-aligned).
+// fp32 partial sums of a K-split bf16 GEMM with `rows` output rows of `cols` columns
+size_t split_part_bytes(int32_t T, int64_t cols) {
+  return T <= kSplitMaxT ? static_cast<size_t>(kMaxSplit) * T * cols * 4 : 0;
+}
+
+// Workspace layout of moe_forward (byte offsets, each 256-aligned). With the router projection
+// (moe_forward_project) the logits and the router GEMM's K-slice sums follow.
 struct Layout {
-  size_t ids, w, offsets, sorted, inv, hist, xperm, h, y, hs, ys, part, part_bytes, end;
+  size_t ids, w, offsets, sorted, inv, hist, xperm, h, y, hs, ys, part, part_bytes, logits, rpart, rpart_bytes, end;
 };
 
-Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
+Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I, bool project = false) {
   Layout L;
   const size_t Tk = static_cast<size_t>(T) * d.top_k;
   size_t off = 256;  // status word
@@ -106,6 +112,9 @@ Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I) {
   L.part_bytes = shared_I > 0 && T <= kSplitMaxT
                      ? static_cast<size_t>(kMaxSplit) * T * std::max(2 * shared_I, d.H) * 4 : 0;
   L.part = take(L.part_bytes);
+  L.logits = take(project ? static_cast<size_t>(T) * d.E * 4 : 0);
+  L.rpart_bytes = project ? split_part_bytes(T, d.E) : 0;
+  L.rpart = take(L.rpart_bytes);
   L.end = off;
   return L;
 }
@@ -180,6 +189,11 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
     p.a = scratch;
     p.a_mma_order = true;
   }
+  // CTA pairs: one pair MMA covers 256 weight rows over two SMs (A in tensor memory only)
+  const bool pair = (flags & MOE_FLAG_GEMM_PAIR) != 0 && asrc == A_TMEM_DQ;
+  auto launch = [&](const GemmProblem& q, int tiles_nt) {
+    return pair ? launch_gemm_pair(q, tiles_nt, sms, s) : launch_gemm_tc(q, asrc, tiles_nt, sms, s);
+  };
   cudaError_t e;
   if (auto_nt && nt == 128) {
     // Many rows per expert on average, but skewed routing leaves a long tail of experts with a
@@ -188,14 +202,14 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
     // its experts, found from the offsets on the device.
     GemmProblem small = p;
     small.max_rows = 32;
-    e = launch_gemm_tc(small, asrc, 32, sms, s);
+    e = launch(small, 32);
     if (e == cudaSuccess) {
       GemmProblem big = p;
       big.min_rows = 33;
-      e = launch_gemm_tc(big, asrc, 128, sms, s);
+      e = launch(big, 128);
     }
   } else {
-    e = launch_gemm_tc(p, asrc, nt, sms, s);
+    e = launch(p, nt);
   }
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(e);
@@ -248,6 +262,48 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   if (split) p.ksplit = pick_ksplit(chunks * ((d.H + 127) / 128), (Is + 255) / 256, sms);
   e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// The router's logit projection, logits fp32 [T][E] = x [T][H] * Wg^T (Wg bf16 [E][H]), on the
+// bf16 tensor-core kernel: the gate's E rows are the weight rows, the tokens the narrow operand,
+// fp32 rows out. Small batches split K as the shared expert does (part may be null: no split).
+moe_status_t run_router(const uint16_t* x, const uint16_t* wg, int32_t T, int32_t E, int32_t H, float* logits,
+                        int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
+  GemmProblem p;
+  p.op = MOE_GEMM_DOWN;
+  p.bf16_weights = true;
+  p.w = wg;
+  p.scales = nullptr;
+  p.a = x;
+  p.offsets = nullptr;
+  p.out = nullptr;
+  p.out_f32 = logits;
+  p.status = status;
+  p.E = 1;
+  p.K = H;
+  p.rows_per_expert = E;
+  p.out_cols = E;
+  p.R = T;
+  p.uniform_rows = T;
+  p.a_mma_order = false;
+  p.out_mma_order = false;
+  const int nt = T <= 16 ? 16 : (T <= 32 ? 32 : 64);
+  if (part != nullptr && T <= kSplitMaxT && !(flags & MOE_FLAG_GEMM_SIMT)) {
+    const int64_t chunks = (T + nt - 1) / nt;
+    p.ksplit = pick_ksplit(chunks * ((E + 127) / 128), (H + 255) / 256, sms);
+    p.partial = part;
+  }
+  const cudaError_t e =
+      (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t check_router(const uint16_t* x, const uint16_t* wg, int32_t T, int32_t E, int32_t H) {
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || E > 1024 || H < 32 || H % 32 || H > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (x == nullptr || wg == nullptr || !aligned16(x) || !aligned16(wg))) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -311,9 +367,13 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags) {
-  (void)flags;
   if (check_dims(d) != MOE_OK || check_T(T, d.top_k) != MOE_OK || shared_I < 0) return 0;
-  return layout(d, T, shared_I).end;
+  return layout(d, T, shared_I, (flags & MOE_FLAG_ROUTER_PROJECT) != 0).end;
+}
+
+size_t moe_router_workspace_size(int32_t T, int32_t E, int32_t H) {
+  if (T < 0 || E < 1 || E > 1024 || H < 32 || H % 32 || H > kMaxDim) return 0;
+  return 256 + align256(split_part_bytes(T, E));
 }
 
 size_t moe_host_staging_size(moe_dims_t d, int32_t T) {
@@ -331,6 +391,32 @@ moe_status_t moe_route(const float* logits, int32_t T, int32_t E, int32_t k, int
   DevInfo di;
   moe_status_t st = current_device(&di);
   if (st != MOE_OK) return st;
+  return cuda_status(launch_route(logits, T, E, k, topk_ids, topk_w, as_stream(stream)));
+}
+
+moe_status_t moe_router_logits(const uint16_t* x, const uint16_t* w_gate, int32_t T, int32_t E, int32_t H,
+                               float* logits, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_router_logits");
+  moe_status_t st = check_router(x, w_gate, T, E, H);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (logits == nullptr || ws == nullptr || !aligned16(logits) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_router_workspace_size(T, E, H)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float* part = split_part_bytes(T, E) > 0 ? reinterpret_cast<float*>(w8 + 256) : nullptr;
+  return run_router(x, w_gate, T, E, H, logits, reinterpret_cast<int*>(w8), flags, di.sms, part, as_stream(stream));
+}
+
+moe_status_t moe_route_project(const uint16_t* x, const uint16_t* w_gate, int32_t T, int32_t E, int32_t H, int32_t k,
+                               float* logits, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                               uint32_t flags, void* stream) {
+  CallRange range_("moe_route_project");
+  if (k < 1 || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (topk_ids == nullptr || topk_w == nullptr)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = moe_router_logits(x, w_gate, T, E, H, logits, ws, ws_bytes, flags, stream);
+  if (st != MOE_OK || T == 0) return st;
   return cuda_status(launch_route(logits, T, E, k, topk_ids, topk_w, as_stream(stream)));
 }
 
@@ -467,6 +553,29 @@ moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x
   if ((st = current_device(&di)) != MOE_OK) return st;
   return forward_device(d, w, x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
                         as_stream(stream));
+}
+
+moe_status_t moe_forward_project(moe_dims_t d, const moe_weights_t* w, const uint16_t* w_gate, const uint16_t* x,
+                                 int32_t T, uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_forward_project");
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights(w, false)) != MOE_OK) return st;
+  if ((st = check_router(x, w_gate, T, d.E, d.H)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (out == nullptr || ws == nullptr || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout(d, T, w->shared_I, true);
+  if (ws_bytes < L.end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  float* logits = reinterpret_cast<float*>(w8 + L.logits);
+  float* part = L.rpart_bytes > 0 ? reinterpret_cast<float*>(w8 + L.rpart) : nullptr;
+  cudaStream_t s = as_stream(stream);
+  st = run_router(x, w_gate, T, d.E, d.H, logits, reinterpret_cast<int*>(w8), flags, di.sms, part, s);
+  if (st != MOE_OK) return st;
+  return forward_device(d, w, x, logits, T, nullptr, out, w8, flags, di.sms, s);
 }
 
 moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host, const float* logits_host,

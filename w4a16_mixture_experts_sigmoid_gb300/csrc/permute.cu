@@ -21,6 +21,8 @@ constexpr int kScatterWarps = 8;  // warps per scatter block, each owns kSeg / 8
 
 __global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ ids, int64_t Tk, int E,
                                                     int32_t* __restrict__ hist, int* status) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   extern __shared__ int32_t h[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
@@ -41,6 +43,8 @@ __global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ 
 // offsets <- exclusive scan of per-expert totals.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, int nblk, int E,
                                                     int32_t* __restrict__ offsets) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   __shared__ int32_t warp_sum[32];
   const int e = threadIdx.x;
   int32_t run = 0;
@@ -84,6 +88,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32
                                                                      const int32_t* __restrict__ offsets,
                                                                      int32_t* __restrict__ sorted_ids,
                                                                      int32_t* __restrict__ inv) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   extern __shared__ int32_t wb[];  // [kScatterWarps][E]: per-warp counts, then per-warp bases
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wb[i] = 0;
@@ -143,6 +149,8 @@ template <bool MMA_ORDER>
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sorted_ids,
                                                      const int32_t* __restrict__ offsets, int E, int R, int H8,
                                                      uint4* __restrict__ xp) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   const int valid = offsets[E];
   for (int row = blockIdx.x; row < R && row < valid; row += gridDim.x) {
     const uint4* src = x + (int64_t)sorted_ids[row] * H8;
@@ -156,6 +164,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
 
 __global__ void __launch_bounds__(256) to_mma_order_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                            int64_t n8) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = to_mma_order8(__ldg(src + i));
 }
@@ -168,9 +178,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* off
                            int32_t* inv_perm, int32_t* hist, int* status, cudaStream_t s) {
   const int64_t Tk = (int64_t)T * k;
   const int nblk = permute_blocks(Tk);
-  count_kernel<<<nblk, 256, sizeof(int32_t) * E, s>>>(ids, Tk, E, hist, status);
-  scan_kernel<<<1, 1024, 0, s>>>(hist, nblk, E, offsets);
-  scatter_kernel<<<nblk, kScatterWarps * 32, sizeof(int32_t) * kScatterWarps * E, s>>>(ids, Tk, k, E, hist, offsets,
+  (void)launch_pdl(count_kernel, dim3(nblk), dim3(256), sizeof(int32_t) * E, s, ids, Tk, E, hist, status);
+  (void)launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, hist, nblk, E, offsets);
+  (void)launch_pdl(scatter_kernel, dim3(nblk), dim3(kScatterWarps * 32), sizeof(int32_t) * kScatterWarps * E, s, ids, Tk, k, E, hist, offsets,
                                                                                      sorted_ids, inv_perm);
   count_launches(3);
   return cudaGetLastError();
@@ -181,10 +191,10 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* sorted_ids, const in
   if (R <= 0) return cudaSuccess;
   const int blocks = R < 4096 ? R : 4096;
   if (mma_order)
-    gather_kernel<true><<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
+    (void)launch_pdl(gather_kernel<true>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
                                                reinterpret_cast<uint4*>(x_perm));
   else
-    gather_kernel<false><<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
+    (void)launch_pdl(gather_kernel<false>, dim3(blocks), dim3(256), 0, s, reinterpret_cast<const uint4*>(x), sorted_ids, offsets, E, R, H / 8,
                                                 reinterpret_cast<uint4*>(x_perm));
   count_launches(1);
   return cudaGetLastError();
@@ -195,7 +205,7 @@ cudaError_t launch_to_mma_order(const uint16_t* src, uint16_t* dst, int64_t rows
   if (n8 <= 0) return cudaSuccess;
   int64_t blocks = (n8 + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  to_mma_order_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(src),
+  (void)launch_pdl(to_mma_order_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, reinterpret_cast<const uint4*>(src),
                                                                     reinterpret_cast<uint4*>(dst), n8);
   count_launches(1);
   return cudaGetLastError();

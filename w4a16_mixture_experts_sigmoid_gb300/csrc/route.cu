@@ -54,6 +54,8 @@ __device__ __forceinline__ bool better(float ka, int ea, float kb, int eb) {
 }
 
 __global__ void sigmoid_kernel(const float* __restrict__ x, int64_t n, float* __restrict__ y) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     y[i] = sigmoid_defined(x[i]);
 }
@@ -69,6 +71,8 @@ template <int SLOTS>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel_reg(const float* __restrict__ logits, int T, int E,
                                                                       int k, int32_t* __restrict__ ids,
                                                                       float* __restrict__ wout) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRouteWarps + warp;
   if (t >= T) return;
@@ -123,6 +127,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel_reg(const float
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel_smem(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* __restrict__ ids,
                                                                   float* __restrict__ wout) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   extern __shared__ float sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float* score = sm + warp * (E + k);
@@ -172,7 +178,7 @@ cudaError_t launch_sigmoid(const float* logits, int64_t n, float* scores, cudaSt
   if (n <= 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 65536) blocks = 65536;
-  sigmoid_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(logits, n, scores);
+  (void)launch_pdl(sigmoid_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, logits, n, scores);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -182,14 +188,14 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int32_t* ids,
   const unsigned blocks = static_cast<unsigned>((T + kRouteWarps - 1) / kRouteWarps);
   const int slots = (E + 31) / 32;
   if (k <= 32 && slots <= 32) {
-    if (slots <= 4) route_kernel_reg<4><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
-    else if (slots <= 8) route_kernel_reg<8><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
-    else if (slots <= 12) route_kernel_reg<12><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
-    else if (slots <= 16) route_kernel_reg<16><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
-    else route_kernel_reg<32><<<blocks, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w);
+    if (slots <= 4) (void)launch_pdl(route_kernel_reg<4>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, T, E, k, ids, w);
+    else if (slots <= 8) (void)launch_pdl(route_kernel_reg<8>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, T, E, k, ids, w);
+    else if (slots <= 12) (void)launch_pdl(route_kernel_reg<12>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, T, E, k, ids, w);
+    else if (slots <= 16) (void)launch_pdl(route_kernel_reg<16>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, T, E, k, ids, w);
+    else (void)launch_pdl(route_kernel_reg<32>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, T, E, k, ids, w);
   } else {
     const size_t smem = sizeof(float) * kRouteWarps * (E + k);
-    route_kernel_smem<<<blocks, kRouteWarps * 32, smem, s>>>(logits, T, E, k, ids, w);
+    (void)launch_pdl(route_kernel_smem, dim3(blocks), dim3(kRouteWarps * 32), smem, s, logits, T, E, k, ids, w);
   }
   count_launches(1);
   return cudaGetLastError();

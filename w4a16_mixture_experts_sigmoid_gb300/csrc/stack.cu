@@ -31,6 +31,8 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // grid-stride over rows; each block reduces one row at a time
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint4* __restrict__ x, int T, int H8, float eps,
                                                                uint4* __restrict__ out) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
   __shared__ float part[kNormThreads / 32];
   __shared__ float rms_s;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const uint4* __re
 cudaError_t launch_rmsnorm(const uint16_t* x, int T, int H, float eps, uint16_t* out, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const int blocks = T < 4096 ? T : 4096;
-  rmsnorm_kernel<<<blocks, kNormThreads, 0, s>>>(reinterpret_cast<const uint4*>(x), T, H / 8, eps,
+  (void)launch_pdl(rmsnorm_kernel, dim3(blocks), dim3(kNormThreads), 0, s, reinterpret_cast<const uint4*>(x), T, H / 8, eps,
                                                  reinterpret_cast<uint4*>(out));
   count_launches(1);
   return cudaGetLastError();
