@@ -42,7 +42,7 @@ __all__ = [
     "unpack_int4", "pack_int4", "dequant", "silu", "expert_mlp",
     "shared_expert", "combine", "moe_layer", "gateup_rows", "down_rows",
     "rmsnorm", "stack_layer", "f32_to_bf16", "expert_int4_params", "EXP_CONSTANTS",
-    "router_logits", "route_projected",
+    "router_logits", "route_projected", "e2m1_to_f32", "e4m3_to_f32", "dequant_fp4", "expert_weights",
 ]
 
 
@@ -242,6 +242,62 @@ def dequant(words: np.ndarray, scale_bits: np.ndarray, group: int = 32) -> np.nd
     return q.reshape(*b.shape[:-1], b.shape[-1] * 2)
 
 
+# ---------------------------------------------------------------------------
+# 4-bit float weights (NVFP4-style checkpoints)
+#
+# The pages name an NVFP4 checkpoint of the previous model and an
+# nvfp4-pack-quantized format ("Kimi k2.5 MLA based eagle3", its test command;
+# "Probing the Depths...", Assumption 2) without spelling it out. The reading
+# taken is the published NVFP4 layout: each weight an E2M1 float (sign, two
+# exponent bits with bias 1, one mantissa bit) in the same nibble positions as
+# the INT4 bank (input 8c + j in bits 4j..4j+3 of word c), one FP8 E4M3 scale
+# per 16 consecutive inputs of a row, and one fp32 scale per matrix and expert:
+#     W[n, i] = e2m1(nibble) * e4m3(scale[n, i // 16]) * g
+# ---------------------------------------------------------------------------
+
+def e2m1_to_f32(nibbles) -> np.ndarray:
+    """E2M1 codes (0..15) -> fp32: (-1)^s * 2^(e-1) * (1 + m/2) for e > 0, (-1)^s * m/2 for e = 0."""
+    n = np.asarray(nibbles).astype(np.int64)
+    s = (n >> 3) & 1
+    e = (n >> 1) & 3
+    m = n & 1
+    mag = np.where(e == 0, 0.5 * m, np.ldexp(1.0 + 0.5 * m, e - 1))
+    return np.where(s == 1, -mag, mag).astype(np.float32)
+
+
+def e4m3_to_f32(bits) -> np.ndarray:
+    """FP8 E4M3 bytes -> fp32: (-1)^s * 2^(e-7) * (1 + m/8) for e > 0, (-1)^s * 2^-6 * m/8 for e = 0;
+    the code with e = 15 and m = 7 is NaN (the format has no infinities)."""
+    b = np.asarray(bits).astype(np.int64)
+    s = (b >> 7) & 1
+    e = (b >> 3) & 15
+    m = b & 7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(s == 1, -mag, mag).astype(np.float32)
+
+
+_BYTE_TO_FP4 = np.array([[e2m1_to_f32(b & 15), e2m1_to_f32(b >> 4)] for b in range(256)], dtype=np.float32)
+
+
+def dequant_fp4(words: np.ndarray, scale_bytes: np.ndarray, gscale, group: int = 16) -> np.ndarray:
+    """W[n, i] = e2m1(nibble) * e4m3(scale[n, i // group]) * g, in fp32 (the first product is exact)."""
+    b = _word_bytes(words)
+    v = _BYTE_TO_FP4[b].reshape(*b.shape[:-1], -1, group)      # [..., groups, group]
+    v *= e4m3_to_f32(scale_bytes)[..., None]
+    v *= np.float32(gscale)
+    return v.reshape(*b.shape[:-1], b.shape[-1] * 2)
+
+
+def expert_weights(layer: dict, e: int):
+    """The fp32 W13 [2I, H] and W2 [H, I] of expert e, dequantised from the layer's format
+    (layer["fmt"] == "nvfp4" for 4-bit floats; INT4 group-32 otherwise)."""
+    if layer.get("fmt") == "nvfp4":
+        return (dequant_fp4(layer["w13"][e], layer["s13"][e], layer["g13"][e]),
+                dequant_fp4(layer["w2"][e], layer["s2"][e], layer["g2"][e]))
+    return dequant(layer["w13"][e], layer["s13"][e]), dequant(layer["w2"][e], layer["s2"][e])
+
+
 def expert_int4_params(H: int, I: int) -> int:
     """Logical int4 weights of one routed expert: W13 [2I, H] plus W2 [H, I]."""
     return 2 * I * H + H * I
@@ -274,6 +330,14 @@ def expert_mlp(x: np.ndarray, w13: np.ndarray, s13: np.ndarray, w2: np.ndarray, 
     W2 = dequant(w2, s2)                     # [H, I]
     y = (h @ W2.T).astype(np.float32)
     return y[0] if single else y
+
+
+def _mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray) -> np.ndarray:
+    """Gated-SiLU MLP of fp32 rows X [n, H] with dequantised fp32 W13 [2I, H], W2 [H, I]."""
+    I = W2.shape[1]
+    gu = (X @ W13.T).astype(np.float32)
+    h = (silu(gu[:, :I]) * gu[:, I:]).astype(np.float32)
+    return (h @ W2.T).astype(np.float32)
 
 
 def shared_expert(x: np.ndarray, wgu_bits: np.ndarray, wd_bits: np.ndarray) -> np.ndarray:
@@ -333,7 +397,8 @@ def moe_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, token
 
     def one_expert(e):
         r, j = np.nonzero(sel == e)
-        y[r, j] = expert_mlp(X[r], layer["w13"][e], layer["s13"][e], layer["w2"][e], layer["s2"][e])
+        W13, W2 = expert_weights(layer, e)
+        y[r, j] = _mlp(X[r], W13, W2)
 
     _map(one_expert, np.unique(sel), workers)
     out = np.zeros((len(tokens), H), dtype=np.float32)
@@ -363,7 +428,7 @@ def gateup_rows(a_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows, work
 
     def one_expert(e):
         sel = np.nonzero(owner == e)[0]
-        W13 = dequant(layer["w13"][e], layer["s13"][e])
+        W13 = expert_weights(layer, e)[0]
         gu = (bf16_to_f32(a_bits[rows[sel]]) @ W13.T).astype(np.float32)
         out[sel] = silu(gu[:, :I]) * gu[:, I:]
 
@@ -380,7 +445,7 @@ def down_rows(h_bits: np.ndarray, offsets: np.ndarray, layer: dict, rows, worker
 
     def one_expert(e):
         sel = np.nonzero(owner == e)[0]
-        out[sel] = bf16_to_f32(h_bits[rows[sel]]) @ dequant(layer["w2"][e], layer["s2"][e]).T
+        out[sel] = bf16_to_f32(h_bits[rows[sel]]) @ expert_weights(layer, e)[1].T
 
     _map(one_expert, np.unique(owner), workers)
     return out

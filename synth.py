@@ -35,7 +35,7 @@ import numpy as np
 _CHUNK = 1 << 22  # elements per independently seeded chunk
 
 # tensor ids: keep every tensor of a layer on its own stream
-TID_W13, TID_S13, TID_W2, TID_S2, TID_SH_GU, TID_SH_D, TID_X, TID_LOGITS, TID_GATE = range(9)
+TID_W13, TID_S13, TID_W2, TID_S2, TID_SH_GU, TID_SH_D, TID_X, TID_LOGITS, TID_GATE, TID_G13, TID_G2 = range(11)
 
 
 @dataclass(frozen=True)
@@ -134,6 +134,35 @@ def make_layer(shape: LayerShape, seed: int = 0, scale_lo: float = 0.005, scale_
         w["sh_gu"] = normal_bf16((2 * Is, H), shared_std, seed, TID_SH_GU)
         w["sh_d"] = normal_bf16((H, Is), shared_std, seed, TID_SH_D)
     return w
+
+
+def uniform_u8(shape, lo: int, hi: int, seed: int, tensor_id: int) -> np.ndarray:
+    """Bytes uniform over the codes lo..hi (inclusive)."""
+    out = np.empty(shape, dtype=np.uint8)
+    return _fill_chunks(out, seed, tensor_id,
+                        lambda g, n: g.integers(lo, hi, size=n, dtype=np.uint8, endpoint=True))
+
+
+def make_layer_fp4(shape: LayerShape, seed: int = 0) -> dict:
+    """Weights of one routed-expert layer in the 4-bit float layout: E2M1 codes packed eight to an
+    int32 word (every code uniform over the sixteen), one FP8 E4M3 scale byte per 16 inputs drawn
+    uniform over the codes 0x30..0x47 (0.5 to 3.75), one fp32 scale per matrix and expert drawn
+    U[0.004, 0.008]: weights of about the INT4 bank's magnitude."""
+    E, H, I = shape.E, shape.H, shape.I
+    assert H % 32 == 0 and I % 32 == 0
+    g13 = np.empty(E, dtype=np.float32)
+    g2 = np.empty(E, dtype=np.float32)
+    _fill_chunks(g13, seed, TID_G13, lambda g, n: np.float32(0.004) + np.float32(0.004) * g.random(n, np.float32))
+    _fill_chunks(g2, seed, TID_G2, lambda g, n: np.float32(0.004) + np.float32(0.004) * g.random(n, np.float32))
+    return {
+        "fmt": "nvfp4",
+        "w13": random_words((E, 2 * I, H // 8), seed, TID_W13),
+        "s13": uniform_u8((E, 2 * I, H // 16), 0x30, 0x47, seed, TID_S13),
+        "g13": g13,
+        "w2": random_words((E, H, I // 8), seed, TID_W2),
+        "s2": uniform_u8((E, H, I // 16), 0x30, 0x47, seed, TID_S2),
+        "g2": g2,
+    }
 
 
 def make_gate(E: int, H: int, seed: int = 0) -> np.ndarray:

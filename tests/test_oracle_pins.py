@@ -518,3 +518,63 @@ def test_identical_gate_rows_tie_to_the_lowest_expert():
         pos = list(ids[t])
         assert pos.index(2) < pos.index(7)
         assert w[t, pos.index(2)] == w[t, pos.index(7)]
+
+
+# ---------------------------------------------------------------------------
+# 4-bit float weights
+# ---------------------------------------------------------------------------
+
+def test_e2m1_codes():
+    """The sixteen E2M1 codes, worked out by hand from sign / 2 exponent bits (bias 1) / 1 mantissa bit."""
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    got = oracle.e2m1_to_f32(np.arange(16))
+    assert list(got) == want
+    assert np.signbit(got[8])
+
+
+def test_e4m3_codes():
+    """Hand-worked E4M3 values: 1.0, the largest finite 448, the smallest normal 2^-6, the smallest
+    subnormal 2^-9, a subnormal with m = 6, a negative, and the NaN code."""
+    cases = {0x38: 1.0, 0x7E: 448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x06: 6 * 2.0 ** -9, 0xC0: -2.0,
+             0x3C: 1.5, 0x40: 2.0, 0x30: 0.5, 0x00: 0.0}
+    for b, v in cases.items():
+        assert float(oracle.e4m3_to_f32(np.array([b]))[0]) == v, hex(b)
+    assert np.isnan(oracle.e4m3_to_f32(np.array([0x7F, 0xFF]))).all()
+    # every finite code is exactly representable in bf16 (8 significant bits): the GPU's exact scale
+    allv = oracle.e4m3_to_f32(np.arange(256))
+    fin = allv[np.isfinite(allv)]
+    assert np.array_equal(oracle.bf16_to_f32(oracle.f32_to_bf16(fin)), fin)
+
+
+def test_fp4_dequant_matches_brute_force():
+    rng = np.random.default_rng(5)
+    words = rng.integers(0, 2 ** 32, size=(3, 8), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    scales = rng.integers(0x20, 0x48, size=(3, 4)).astype(np.uint8)
+    g = np.float32(0.37)
+    got = oracle.dequant_fp4(words, scales, g)
+    e2m1 = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    for n in range(3):
+        for c in range(8):
+            u = int(words[n, c]) & 0xFFFFFFFF
+            for j in range(8):
+                i = 8 * c + j
+                sb = int(scales[n, i // 16])
+                e, m = (sb >> 3) & 15, sb & 7
+                sv = (m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+                want = np.float32(e2m1[(u >> (4 * j)) & 15] * sv) * g     # exact product, one fp32 rounding by g
+                assert got[n, i] == np.float32(want), (n, i)
+
+
+def test_fp4_layer_single_expert_equals_dense_brute_force():
+    import synth
+    shape = synth.LayerShape(E=1, top_k=1, H=64, I=32)
+    layer = synth.make_layer_fp4(shape, seed=3)
+    x_bits, logits = synth.make_tokens(2, 64, 1, seed=4)
+    res = oracle.moe_layer(x_bits, logits, layer, k=1)
+    W13, W2 = oracle.expert_weights(layer, 0)
+    for t in range(2):
+        x = [bf16_bits_to_float(b) for b in x_bits[t]]
+        gu = [sum(float(a) * b for a, b in zip(row, x)) for row in W13]
+        h = [gu[i] / (1.0 + math.exp(-gu[i])) * gu[32 + i] for i in range(32)]
+        ref = np.array([sum(float(a) * b for a, b in zip(row, h)) for row in W2])
+        assert np.abs(res["out"][t] - ref).max() <= 1e-5 * np.sqrt(np.mean(ref ** 2))

@@ -4,6 +4,8 @@ give, call after call, with no device memory taken or freed by the call.
 
 Collected last (file name) so that it also runs after every other GPU test in
 the same process; it must pass alone as well."""
+import gc
+
 import numpy as np
 import pytest
 
@@ -52,16 +54,24 @@ def test_static_scratch_matches_moe_permute_twice_without_allocating(cuda_lib, T
         want = _with_workspace(B, ids_d, x, T, E, k, H, flags)
         off, srt, inv, xp = _outputs(T, E, k, H)
         torch.cuda.synchronize()
-        used0 = torch.cuda.memory_allocated()
-        free0 = torch.cuda.mem_get_info()[0]
-        B.moe_permute_static_scratch(ids_d, T, E, k, off, srt, inv, x, H, xp, status, flags)
-        torch.cuda.synchronize()
+        # garbage left by earlier tests is freed now, not by a collection inside the measured call
+        gc.collect()
+        gc.disable()
+        try:
+            used0 = torch.cuda.memory_allocated()
+            free0 = torch.cuda.mem_get_info()[0]
+            B.moe_permute_static_scratch(ids_d, T, E, k, off, srt, inv, x, H, xp, status, flags)
+            torch.cuda.synchronize()
+            used1 = torch.cuda.memory_allocated()
+            free1 = torch.cuda.mem_get_info()[0]
+        finally:
+            gc.enable()
         # nothing of this process's memory came or went (the strict check) ...
-        assert torch.cuda.memory_allocated() == used0
+        assert used1 == used0
         if call == 1:
             # ... and, after the first call's set-up, the device's free memory did not drop by an
             # allocation's worth; other processes may share this GPU, so this one is approximate
-            assert torch.cuda.mem_get_info()[0] >= free0 - (2 << 20)
+            assert free1 >= free0 - (2 << 20)
         assert B.moe_check_status(status) == B.MOE_OK
         got = [host(t) for t in (off, srt, inv, xp)]
         for name, g, w in zip(("expert_offsets", "sorted_token_ids", "inv_perm", "x_perm"), got, want):
