@@ -54,6 +54,10 @@ WORKLOADS = {
     # 12 full-size layers (114 GB of int4 + scales) chained as x <- x + MoE_l(RMSNorm(x)); layer l's weights
     # and router logits use seed l, x seed 0
     "stack12_t256": dict(shape=synth.FULL, T=256, skew=None, layers=12),
+    # the same decode layer with 4-bit float weights: E2M1 codes, an E4M3 scale per 16 inputs, an fp32
+    # scale per matrix and expert (the same 24.77 MB per expert)
+    "decode_t64_nvfp4": dict(shape=synth.FULL, T=64, skew=None, fmt="nvfp4"),
+    "prefill_t4096_zipf_nvfp4": dict(shape=synth.FULL, T=4096, skew=1.1, fmt="nvfp4"),
 }
 
 
@@ -92,8 +96,10 @@ def kernel_roofline(kernel, alg_bytes, flops, kernel_ms, traffic, hbm, bf16_sus,
 
 def workload_desc(name, w):
     s = w["shape"]
-    txt = (f"{name}: routed MoE layer E={s.E} top-{s.top_k} H={s.H} I={s.I}, int4 group-32 weights + bf16 "
-           f"scales, bf16 activations, T={w['T']} tokens")
+    wdesc = ("E2M1 4-bit float weights + an E4M3 scale per 16 + an fp32 scale per matrix"
+             if w.get("fmt") == "nvfp4" else "int4 group-32 weights + bf16 scales")
+    txt = (f"{name}: routed MoE layer E={s.E} top-{s.top_k} H={s.H} I={s.I}, {wdesc}, bf16 activations, "
+           f"T={w['T']} tokens")
     if w.get("layers", 1) > 1:
         txt = (f"{name}: {w['layers']} routed MoE layers E={s.E} top-{s.top_k} H={s.H} I={s.I} chained as "
                f"x <- x + MoE_l(RMSNorm(x)), int4 group-32 weights + bf16 scales, bf16 activations, "
@@ -109,7 +115,7 @@ def workload_desc(name, w):
 
 def make_inputs(w, seed=0):
     s = w["shape"]
-    arrays = synth.make_layer(s, seed=seed)
+    arrays = synth.make_layer_fp4(s, seed=seed) if w.get("fmt") == "nvfp4" else synth.make_layer(s, seed=seed)
     bias = synth.zipf_bias(s.E, w["T"], s.top_k, w["skew"], seed) if w["skew"] else None
     x, logits = synth.make_tokens(w["T"], s.H, s.E, seed=seed, bias=bias)
     return arrays, x, logits
@@ -308,7 +314,8 @@ def run_reference(args):
         t, j = units[i % len(units)]
         xf = oracle.bf16_to_f32(x[t])
         e = int(ids[t, j])
-        y = oracle.expert_mlp(xf, arrays["w13"][e], arrays["s13"][e], arrays["w2"][e], arrays["s2"][e])
+        W13, W2 = oracle.expert_weights(arrays, e)      # dequantised from the workload's weight format
+        y = oracle.mlp(xf[None], W13, W2)[0]
         return rw[t, j] * y
 
     for i in range(args.warmup):
@@ -340,7 +347,7 @@ def run_ours(args):
     import __graft_entry__
     __graft_entry__.build()
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
-    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer
+    from w4a16_mixture_experts_sigmoid_gb300.layer import MoeFp4Layer, MoeW4A16Layer
 
     world, rank, local = dist_setup(args.gpus)
     torch.cuda.set_device(local)
@@ -348,8 +355,10 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     s = w["shape"]
     T = w["T"]
+    fp4 = w.get("fmt") == "nvfp4"
     arrays, x, logits = make_inputs(w, seed=0)
-    layer = MoeW4A16Layer.from_arrays(s, arrays, device=dev)
+    layer = (MoeFp4Layer if fp4 else MoeW4A16Layer).from_arrays(s, arrays, device=dev)
+    gemm_call = B.moe_fp4_grouped_gemm if fp4 else B.moe_w4a16_grouped_gemm
     xd = torch.from_numpy(x.view(np.int16)).to(dev)
     ld = torch.from_numpy(logits).to(dev)
     out = torch.empty((T, s.H), dtype=torch.int16, device=dev)
@@ -431,11 +440,9 @@ def run_ours(args):
         E_[1].record(stream)
         B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp, order)
         E_[2].record(stream)
-        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp,
-                                 flags | order)
+        gemm_call(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp, flags | order)
         E_[3].record(stream)
-        B.moe_w4a16_grouped_gemm(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp,
-                                 flags | order | B.MOE_FLAG_OUT_F32)
+        gemm_call(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags | order | B.MOE_FLAG_OUT_F32)
         E_[4].record(stream)
         j = 5
         if ys is not None:
@@ -481,21 +488,33 @@ def run_ours(args):
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
     lh = torch.from_numpy(logits).pin_memory()
     oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
+    xe, le = torch.empty_like(xd), torch.empty_like(ld)
+
+    def e2e_step():
+        if fp4:   # pinned host buffers through torch copies on the stream around moe_forward_fp4
+            xe.copy_(xh, non_blocking=True)
+            le.copy_(lh, non_blocking=True)
+            layer.forward(xe, le, out=out, flags=flags)
+            oh.copy_(out, non_blocking=True)
+        else:
+            layer.forward_host(xh, lh, oh, flags=flags)
+
     for _ in range(3):
-        layer.forward_host(xh, lh, oh, flags=flags)
+        e2e_step()
     torch.cuda.synchronize(dev)
     esteps = max(10, min(args.steps, 200))
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for _ in range(esteps):
-        layer.forward_host(xh, lh, oh, flags=flags)
+        e2e_step()
         torch.cuda.current_stream(dev).synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / esteps, dev)
     e2e = {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": x.nbytes + logits.nbytes,
            "d2h_bytes_per_step": T * s.H * 2, "ms_per_step": e2e_s * 1e3,
-           "note": "moe_forward_host: pinned host x/logits -> device, layer, result -> pinned host, stream "
-                   "synchronised every step"}
+           "note": ("pinned host x/logits -> device (torch copies on the stream), moe_forward_fp4, result -> "
+                    "pinned host" if fp4 else "moe_forward_host: pinned host x/logits -> device, layer, result -> "
+                    "pinned host") + ", stream synchronised every step"}
 
     if rank != 0:
         return

@@ -92,6 +92,32 @@ typedef struct {
   int32_t shared_I;
 } moe_weights_t;
 
+/* Weights of one layer in the 4-bit float format (NVFP4-style checkpoints).
+ * Passage: "Kimi k2.5 MLA based eagle3", test plan (an NVFP4 checkpoint of the
+ * model family) and "Probing the Depths: Verifying SGLang Compatibility for
+ * Kimi K2.6 Deployment", Assumption 2 (nvfp4_pack_quantized). The pages name
+ * the format without spelling it out; the reading is the published NVFP4
+ * layout. Per expert e:
+ *   w13_packed[e] : int32 [2I][H/8]  E2M1 codes (sign, 2 exponent bits with
+ *                   bias 1, 1 mantissa bit) in the INT4 bank's nibble places
+ *   w13_scale[e]  : uint8 [2I][H/16] FP8 E4M3 scale of each 16 inputs
+ *   w13_gscale[e] : fp32             scale of the whole matrix
+ *   w2_packed[e]  : int32 [H][I/8], w2_scale[e] : uint8 [H][I/16], w2_gscale[e]
+ *   W[n][i] = e2m1(code) * e4m3(scale[n][i/16]) * gscale
+ * The shared expert is the bf16 one of moe_weights_t. moe_dims_t.group must
+ * be 16 for this format. */
+typedef struct {
+  const int32_t* w13_packed;
+  const uint8_t* w13_scale;
+  const float* w13_gscale;
+  const int32_t* w2_packed;
+  const uint8_t* w2_scale;
+  const float* w2_gscale;
+  const uint16_t* shared_wgu;
+  const uint16_t* shared_wd;
+  int32_t shared_I;
+} moe_weights_fp4_t;
+
 /* Grouped GEMM operations. */
 #define MOE_GEMM_GATEUP_SILU 0   /* h[r, :] = SiLU(W_gate a[r]) .* (W_up a[r]), out [R][I] */
 #define MOE_GEMM_DOWN 1          /* y[r, :] = W2 a[r],                          out [R][H] */
@@ -260,6 +286,16 @@ MOE_API moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_
                                     const int32_t* expert_offsets, uint16_t* out_rows,
                                     void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* moe_w4a16_grouped_gemm over 4-bit float weights (moe_weights_fp4_t, group
+ * 16): each E2M1 code times its E4M3 scale is exact in bf16, the products sum
+ * in fp32 on the tensor cores and the matrix scale multiplies the fp32 sums.
+ * Same arguments, flags and workspace as moe_w4a16_grouped_gemm, except that
+ * MOE_FLAG_GEMM_SIMT and MOE_FLAG_A_SMEM return MOE_ERR_UNSUPPORTED_SHAPE. */
+MOE_API moe_status_t moe_fp4_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_fp4_t* w,
+                                  const uint16_t* a_rows, int32_t T, const int32_t* expert_offsets,
+                                  uint16_t* out_rows, void* ws, size_t ws_bytes, uint32_t flags,
+                                  void* stream);
+
 /* The dense bf16 shared expert. Passage: "Kimi-K2.6" catalog page, GEOMETRY
  * (n_shared_experts 1, moe_intermediate_size 2048) and PARAMS (the BF16
  * share of the checkpoint, outside the INT4 bank).
@@ -301,6 +337,12 @@ MOE_API moe_status_t moe_combine_f32(const float* y_rows, const int32_t* inv_per
 MOE_API moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x, const float* logits,
                          int32_t T, uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags,
                          void* stream);
+
+/* moe_forward with 4-bit float routed experts (and the optional bf16 shared
+ * expert): workspace, flags and results as moe_forward (d.group == 16). */
+MOE_API moe_status_t moe_forward_fp4(moe_dims_t d, const moe_weights_fp4_t* w, const uint16_t* x,
+                             const float* logits, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
+                             uint32_t flags, void* stream);
 
 /* The whole layer from the token activations alone: the router logits are
  * projected from x with w_gate (bf16 [E][H], as moe_router_logits) into the

@@ -42,7 +42,7 @@ __all__ = [
     "unpack_int4", "pack_int4", "dequant", "silu", "expert_mlp",
     "shared_expert", "combine", "moe_layer", "gateup_rows", "down_rows",
     "rmsnorm", "stack_layer", "f32_to_bf16", "expert_int4_params", "EXP_CONSTANTS",
-    "router_logits", "route_projected", "e2m1_to_f32", "e4m3_to_f32", "dequant_fp4", "expert_weights",
+    "router_logits", "route_projected", "mlp", "e2m1_to_f32", "e4m3_to_f32", "dequant_fp4", "expert_weights",
 ]
 
 
@@ -332,7 +332,7 @@ def expert_mlp(x: np.ndarray, w13: np.ndarray, s13: np.ndarray, w2: np.ndarray, 
     return y[0] if single else y
 
 
-def _mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray) -> np.ndarray:
+def mlp(X: np.ndarray, W13: np.ndarray, W2: np.ndarray) -> np.ndarray:
     """Gated-SiLU MLP of fp32 rows X [n, H] with dequantised fp32 W13 [2I, H], W2 [H, I]."""
     I = W2.shape[1]
     gu = (X @ W13.T).astype(np.float32)
@@ -398,7 +398,7 @@ def moe_layer(x_bits: np.ndarray, logits: np.ndarray, layer: dict, k: int, token
     def one_expert(e):
         r, j = np.nonzero(sel == e)
         W13, W2 = expert_weights(layer, e)
-        y[r, j] = _mlp(X[r], W13, W2)
+        y[r, j] = mlp(X[r], W13, W2)
 
     _map(one_expert, np.unique(sel), workers)
     out = np.zeros((len(tokens), H), dtype=np.float32)

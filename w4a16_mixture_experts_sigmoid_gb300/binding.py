@@ -49,6 +49,12 @@ class moe_weights_t(Structure):
                 ("shared_I", c_int32)]
 
 
+class moe_weights_fp4_t(Structure):
+    _fields_ = [("w13_packed", c_void_p), ("w13_scale", c_void_p), ("w13_gscale", c_void_p),
+                ("w2_packed", c_void_p), ("w2_scale", c_void_p), ("w2_gscale", c_void_p),
+                ("shared_wgu", c_void_p), ("shared_wd", c_void_p), ("shared_I", c_int32)]
+
+
 # name -> (restype, argtypes); every symbol include/moe_w4a16.h declares
 SIGNATURES = {
     "moe_status_string": (c_char_p, [c_int32]),
@@ -60,6 +66,10 @@ SIGNATURES = {
                                     c_uint32, c_void_p]),
     "moe_route_project": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
                                     c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_fp4_grouped_gemm": (c_int32, [c_int32, moe_dims_t, POINTER(moe_weights_fp4_t), c_void_p, c_int32,
+                                       c_void_p, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_forward_fp4": (c_int32, [moe_dims_t, POINTER(moe_weights_fp4_t), c_void_p, c_void_p, c_int32, c_void_p,
+                                  c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_forward_project": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_void_p, c_int32, c_void_p,
                                       c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
@@ -195,6 +205,26 @@ def moe_route_project(x, w_gate, T: int, E: int, H: int, k: int, logits, topk_id
     _check(load().moe_route_project(_dptr(x), _dptr(w_gate), T, E, H, k, _dptr(logits), _dptr(topk_ids),
                                     _dptr(topk_w), _dptr(ws), _nbytes(ws), flags, _stream(stream)),
            "moe_route_project")
+
+
+def weights_fp4(w13, s13, g13, w2, s2, g2, sh_gu=None, sh_d=None) -> moe_weights_fp4_t:
+    """moe_weights_fp4_t of device tensors (scales uint8, matrix scales fp32 [E])."""
+    Is = 0 if sh_d is None else int(sh_d.shape[1])
+    return moe_weights_fp4_t(_dptr(w13), _dptr(s13), _dptr(g13), _dptr(w2), _dptr(s2), _dptr(g2), _dptr(sh_gu),
+                             _dptr(sh_d), Is)
+
+
+def moe_fp4_grouped_gemm(op: int, d: moe_dims_t, w: moe_weights_fp4_t, a_rows, T: int, expert_offsets, out_rows,
+                         ws, flags: int = 0, stream=None) -> None:
+    _check(load().moe_fp4_grouped_gemm(op, d, ctypes.byref(w), _dptr(a_rows), T, _dptr(expert_offsets),
+                                       _dptr(out_rows), _dptr(ws), _nbytes(ws), flags, _stream(stream)),
+           "moe_fp4_grouped_gemm")
+
+
+def moe_forward_fp4(d: moe_dims_t, w: moe_weights_fp4_t, x, logits, T: int, out, ws, flags: int = 0,
+                    stream=None) -> None:
+    _check(load().moe_forward_fp4(d, ctypes.byref(w), _dptr(x), _dptr(logits), T, _dptr(out), _dptr(ws), _nbytes(ws),
+                                  flags, _stream(stream)), "moe_forward_fp4")
 
 
 def moe_forward_project(d: moe_dims_t, w: moe_weights_t, w_gate, x, T: int, out, ws, flags: int = 0,

@@ -64,7 +64,7 @@ struct PairCfg {
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-template <int OP, int NT>
+template <int OP, int NT, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   using C = PairCfg<NT>;
   constexpr int SW = C::kWStages;
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         if (!warp_wait(&wempty[sw], ((g / SW) & 1) ^ 1, p, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + sw * C::kWStage;
         uint8_t* ss = sa + C::kAStage;
-        if (!p.scale_tma) {
+        if (!p.scale_tma && FMT == WFMT_INT4) {
           uint16_t* sc = reinterpret_cast<uint16_t*>(ss);
           for (int r = lane; r < BM; r += 32) {
             const int grow = (r < 64) ? grow_lo + r : grow_hi + (r - 64);
@@ -189,6 +189,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
               uint16_t v = 0;
               if (gi < kg && grow < p.rows_total) v = p.scales[static_cast<int64_t>(grow) * kg + gi];
               sc[r * 8 + q] = v;
+            }
+          }
+        } else if (!p.scale_tma) {
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales);
+          const int kb16 = p.K / 16;
+          for (int r = lane; r < BM; r += 32) {
+            const int grow = (r < 64) ? grow_lo + r : grow_hi + (r - 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const int gi = ks * 16 + q;
+              uint8_t v = 0;
+              if (gi < kb16 && grow < p.rows_total) v = src[static_cast<int64_t>(grow) * kb16 + gi];
+              ss[r * 16 + q] = v;
             }
           }
         }
@@ -329,8 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
         uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
 #pragma unroll
-        for (int c = 0; c < kPreChunks; ++c)
-          dequant_group(wv[c], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), pre[c]);
+        for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT>(wv[c], sw4, c, pre[c]);
         if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
@@ -345,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           for (int cc = 0; cc < 4; ++cc) {
             const int c = half * 4 + cc;
             uint32_t dqc[16];
-            if (c >= kPreChunks) dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dqc);
+            if (c >= kPreChunks) dequant_chunk<FMT>(wv[cc], sw4, c, dqc);
             const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
             tmem_st8(lane_base + b * 128 + c * 16, dq);
             tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
@@ -391,6 +403,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
+        }
+        if (FMT == WFMT_FP4) {
+          const float gs = __ldg(p.gscale + ti.e);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * gs);
         }
         if (OP == MOE_GEMM_GATEUP_SILU) {
           float u[16];
@@ -441,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 }
 
 // Clusters of two that can be resident at once, per device ordinal and kernel.
-template <int OP, int NT>
+template <int OP, int NT, int FMT>
 int max_pairs(cudaStream_t s, int num_sms) {
   static std::atomic<int> cached[64];
   int dev = 0;
@@ -461,7 +478,7 @@ int max_pairs(cudaStream_t s, int num_sms) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<OP, NT>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<OP, NT, FMT>, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = num_sms / 2;
   }
@@ -469,7 +486,7 @@ int max_pairs(cudaStream_t s, int num_sms) {
   return n;
 }
 
-template <int OP, int NT>
+template <int OP, int NT, int FMT>
 cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaStream_t s) {
   using C = PairCfg<NT>;
   static std::atomic<uint64_t> opted_in{0};
@@ -478,12 +495,12 @@ cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaS
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || !(opted_in.load() & bit)) {
-    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<OP, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<OP, NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  const int cap = max_pairs<OP, NT>(s, num_sms);
+  const int cap = max_pairs<OP, NT, FMT>(s, num_sms);
   const int pairs = static_cast<int>(pair_tiles < cap ? pair_tiles : cap);
   if (pairs <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
@@ -500,19 +517,19 @@ cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaS
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<OP, NT>, prm);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<OP, NT, FMT>, prm);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int OP>
+template <int OP, int FMT>
 cudaError_t dispatch_pair(const TcParams& prm, int nt, int64_t pair_tiles, int num_sms, cudaStream_t s) {
   switch (nt) {
-    case 16: return run_pair<OP, 16>(prm, pair_tiles, num_sms, s);
-    case 32: return run_pair<OP, 32>(prm, pair_tiles, num_sms, s);
-    case 64: return run_pair<OP, 64>(prm, pair_tiles, num_sms, s);
-    case 128: return run_pair<OP, 128>(prm, pair_tiles, num_sms, s);
+    case 16: return run_pair<OP, 16, FMT>(prm, pair_tiles, num_sms, s);
+    case 32: return run_pair<OP, 32, FMT>(prm, pair_tiles, num_sms, s);
+    case 64: return run_pair<OP, 64, FMT>(prm, pair_tiles, num_sms, s);
+    case 128: return run_pair<OP, 128, FMT>(prm, pair_tiles, num_sms, s);
   }
   return cudaErrorNotSupported;
 }
@@ -523,6 +540,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int nt, int num_sms, cudaStre
   if (p.R <= 0) return cudaSuccess;
   if (p.bf16_weights || !p.a_mma_order || p.ksplit != 1) return cudaErrorNotSupported;
   if (p.E > kMaxE || num_sms < 2) return cudaErrorNotSupported;
+  if (p.wfmt == WFMT_FP4 && p.gscale == nullptr) return cudaErrorInvalidValue;
   TcParams prm;
   memset(&prm, 0, sizeof(prm));
   const int groups = p.uniform_rows >= 0 ? 1 : p.E;
@@ -530,15 +548,14 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int nt, int num_sms, cudaStre
   bool ok = make_map_2d(&prm.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, p.w, p.K / 8, rows_total, p.K / 2, BK / 8, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B);
   prm.scale_tma = (p.K % 256 == 0) ? 1 : 0;
-  if (ok && prm.scale_tma)
-    ok = make_map_2d(&prm.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.scales, p.K / 32, rows_total, p.K / 16, 8, 64,
-                     CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (ok && prm.scale_tma) ok = make_scale_map(&prm.tm_s, p.wfmt, p.scales, p.K, rows_total);
   // each CTA loads half of a tile's token rows
   if (ok)
     ok = make_map_2d(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.R, 2ull * p.K, KSUB, nt / 2,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   prm.scales = p.scales;
+  prm.gscale = p.gscale;
   prm.offsets = p.offsets;
   prm.out = p.out;
   prm.out_f32 = (p.op == MOE_GEMM_DOWN) ? p.out_f32 : nullptr;
@@ -559,8 +576,12 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int nt, int num_sms, cudaStre
   const int n_wt = (p.op == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 127) / 128 : (p.rows_per_expert + 255) / 256;
   const int64_t chunks = static_cast<int64_t>(p.R) / nt + (groups < p.R ? groups : p.R);
   const int64_t pair_tiles = chunks * n_wt;
-  return (p.op == MOE_GEMM_GATEUP_SILU) ? dispatch_pair<MOE_GEMM_GATEUP_SILU>(prm, nt, pair_tiles, num_sms, s)
-                                        : dispatch_pair<MOE_GEMM_DOWN>(prm, nt, pair_tiles, num_sms, s);
+  if (p.wfmt == WFMT_FP4)
+    return (p.op == MOE_GEMM_GATEUP_SILU)
+               ? dispatch_pair<MOE_GEMM_GATEUP_SILU, WFMT_FP4>(prm, nt, pair_tiles, num_sms, s)
+               : dispatch_pair<MOE_GEMM_DOWN, WFMT_FP4>(prm, nt, pair_tiles, num_sms, s);
+  return (p.op == MOE_GEMM_GATEUP_SILU) ? dispatch_pair<MOE_GEMM_GATEUP_SILU, WFMT_INT4>(prm, nt, pair_tiles, num_sms, s)
+                                        : dispatch_pair<MOE_GEMM_DOWN, WFMT_INT4>(prm, nt, pair_tiles, num_sms, s);
 }
 
 }  // namespace moe

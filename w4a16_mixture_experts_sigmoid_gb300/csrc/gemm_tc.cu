@@ -108,7 +108,7 @@ struct Cfg {
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-template <int OP, int ASRC, int NT>
+template <int OP, int ASRC, int NT, int FMT = WFMT_INT4>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<ASRC, NT>;
   constexpr int SW = C::kWStages;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (!warp_wait(&wempty[sw], ((g / SW) & 1) ^ 1, p, abort_flag)) { ok = false; break; }
         uint8_t* sa = smem + sw * C::kWStage;
         uint8_t* ss = sa + C::kAStage;
-        if (C::kDq && !p.scale_tma) {
+        if (C::kDq && !p.scale_tma && FMT == WFMT_INT4) {
           // scales by plain loads (row stride not 16-byte aligned): lane owns rows lane + 32 r
           uint16_t* sc = reinterpret_cast<uint16_t*>(ss);
           for (int r = lane; r < BM; r += 32) {
@@ -245,6 +245,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               uint16_t v = 0;
               if (gi < kg && grow < p.rows_total) v = p.scales[static_cast<int64_t>(grow) * kg + gi];
               sc[r * 8 + q] = v;
+            }
+          }
+        } else if (C::kDq && !p.scale_tma) {
+          // E4M3 scale bytes, one per 16 inputs: 16 a row per stage
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(p.scales);
+          const int kb16 = p.K / 16;
+          for (int r = lane; r < BM; r += 32) {
+            const int grow = (r < 64) ? grow_lo + r : grow_hi + (r - 64);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const int gi = (kb + ks) * 16 + q;
+              uint8_t v = 0;
+              if (gi < kb16 && grow < p.rows_total) v = src[static_cast<int64_t>(grow) * kb16 + gi];
+              ss[r * 16 + q] = v;
             }
           }
         }
@@ -416,8 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
           uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
 #pragma unroll
-          for (int c = 0; c < kPreChunks; ++c)
-            dequant_group(wv[c], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), pre[c]);
+          for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT>(wv[c], sw4, c, pre[c]);
           if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -433,8 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             for (int cc = 0; cc < 4; ++cc) {
               const int c = half * 4 + cc;
               uint32_t dqc[16];
-              if (c >= kPreChunks)
-                dequant_group(wv[cc], (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), dqc);
+              if (c >= kPreChunks) dequant_chunk<FMT>(wv[cc], sw4, c, dqc);
               const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
               if (ASRC == A_TMEM_DQ) {
                 tmem_st8(lane_base + b * 128 + c * 16, dq);
@@ -486,6 +498,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
+        }
+        if (FMT == WFMT_FP4) {
+          const float gs = __ldg(p.gscale + ti.e);   // the expert's fp32 matrix scale
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * gs);
         }
         if (ASRC == A_SMEM_BF16 && ksplit > 1) {
           // one K slice: its raw fp32 sums go to the partial buffer, each lane its own weight row
@@ -560,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 // host side
 // ---------------------------------------------------------------------------
 
-template <int OP, int ASRC, int NT>
+template <int OP, int ASRC, int NT, int FMT = WFMT_INT4>
 cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
   using C = Cfg<ASRC, NT>;
   // the shared-memory opt-in is per device: remember it per device ordinal
@@ -570,12 +587,12 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || !(opted_in.load() & bit)) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<OP, ASRC, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<OP, ASRC, NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  (void)launch_pdl(tc_gemm_kernel<OP, ASRC, NT>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, prm);
+  (void)launch_pdl(tc_gemm_kernel<OP, ASRC, NT, FMT>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, prm);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -609,7 +626,17 @@ __global__ void __launch_bounds__(256) splitk_finish_kernel(const float* __restr
 }
 
 template <int OP>
-cudaError_t dispatch(const TcParams& prm, int asrc, int nt, int grid, cudaStream_t s) {
+cudaError_t dispatch(const TcParams& prm, int asrc, int nt, int grid, int wfmt, cudaStream_t s) {
+  if (wfmt == WFMT_FP4) {
+    if (asrc != A_TMEM_DQ) return cudaErrorNotSupported;
+    switch (nt) {
+      case 16: return run<OP, A_TMEM_DQ, 16, WFMT_FP4>(prm, grid, s);
+      case 32: return run<OP, A_TMEM_DQ, 32, WFMT_FP4>(prm, grid, s);
+      case 64: return run<OP, A_TMEM_DQ, 64, WFMT_FP4>(prm, grid, s);
+      case 128: return run<OP, A_TMEM_DQ, 128, WFMT_FP4>(prm, grid, s);
+    }
+    return cudaErrorNotSupported;
+  }
   switch (asrc) {
     case A_TMEM_DQ:
       switch (nt) {
@@ -657,17 +684,18 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
                      CU_TENSOR_MAP_SWIZZLE_128B);
     prm.scale_tma = (p.K % 256 == 0) ? 1 : 0;
     if (ok && prm.scale_tma)
-      ok = make_map_2d(&prm.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.scales, p.K / 32, rows_total, p.K / 16, 8, 64,
-                       CU_TENSOR_MAP_SWIZZLE_NONE);
+      ok = make_scale_map(&prm.tm_s, p.wfmt, p.scales, p.K, rows_total);
   }
   if (ok)
     ok = make_map_2d(&prm.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.a, p.K, p.R, 2ull * p.K, KSUB, nt,
                      CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   prm.scales = p.scales;
+  prm.gscale = p.gscale;
   prm.offsets = p.offsets;
   prm.out = p.out;
   prm.out_f32 = (p.op == MOE_GEMM_DOWN) ? p.out_f32 : nullptr;
+  if (p.wfmt == WFMT_FP4 && (p.bf16_weights || p.gscale == nullptr)) return cudaErrorInvalidValue;
   prm.status = p.status;
   prm.E = p.E;
   prm.K = p.K;
@@ -690,8 +718,8 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   const int64_t chunks = static_cast<int64_t>(p.R) / nt + (groups < p.R ? groups : p.R);
   const int64_t tiles = chunks * n_wt * p.ksplit;
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  cudaError_t e = (p.op == MOE_GEMM_GATEUP_SILU) ? dispatch<MOE_GEMM_GATEUP_SILU>(prm, asrc, nt, grid, s)
-                                                 : dispatch<MOE_GEMM_DOWN>(prm, asrc, nt, grid, s);
+  cudaError_t e = (p.op == MOE_GEMM_GATEUP_SILU) ? dispatch<MOE_GEMM_GATEUP_SILU>(prm, asrc, nt, grid, p.wfmt, s)
+                                                 : dispatch<MOE_GEMM_DOWN>(prm, asrc, nt, grid, p.wfmt, s);
   if (e != cudaSuccess || p.ksplit == 1) return e;
   const int64_t n = static_cast<int64_t>(p.R) * p.out_cols;
   const int fb = static_cast<int>((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);

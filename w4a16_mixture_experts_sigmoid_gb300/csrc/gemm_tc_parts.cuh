@@ -31,7 +31,8 @@ struct TcParams {
   CUtensorMap tm_w;  // int4 words [rows_total][K/8] (box 32 x 64) or bf16 weights [rows_total][K] (box 64 x 16)
   CUtensorMap tm_s;  // bf16 scales [rows_total][K/32] (box 8 x 64), when scale_tma
   CUtensorMap tm_b;  // bf16 token rows [R][K] (box 64 x NT)
-  const uint16_t* scales;
+  const uint16_t* scales;  // int4: bf16 [rows][K/32]; fp4: E4M3 bytes [rows][K/16] (read through a byte pointer)
+  const float* gscale;     // fp4: per-expert fp32 scale, applied to the fp32 sums in the epilogue
   const int32_t* offsets;
   uint16_t* out;
   float* out_f32;          // down: fp32 rows instead of bf16 `out`, when set
@@ -113,6 +114,51 @@ __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t scale_bi
   }
 }
 
+// The 4-bit float format: one 16-byte chunk of E2M1 codes = four words = 32 inputs, two blocks of
+// 16 with their own scale, -> 16 bf16x2 registers in MMA K order (register 4i+m: inputs 8i+m and
+// 8i+m+4, as dequant_group). A code's magnitude bits (two exponent bits, one mantissa bit) moved to
+// bf16 bits 6..8 and its sign to bit 15 read as the code's value times 2^-126 (the codes +-0.5 as
+// bf16 subnormals); one packed multiply by 2^126 makes the value and one by the block's scale the
+// weight. Both products are exact: E2M1 values have two significant bits and E4M3 scales four.
+__device__ __forceinline__ void dequant_group_fp4(const uint4& wv, uint32_t s2_blk0, uint32_t s2_blk1,
+                                                  uint32_t* out16) {
+  const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t s2 = (i < 2) ? s2_blk0 : s2_blk1;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t t = w4[i] >> (4 * m);
+      const uint32_t bits = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
+      uint32_t v;
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(bits), "r"(0x7E807E80u));   // 0x7E80 = bf16 2^126
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(v), "r"(s2));
+    }
+  }
+}
+
+// E4M3 scale byte -> its exact value as bf16 in both halves of a register. The byte's exponent and
+// mantissa bits moved to bf16 bits 4..10 and its sign to bit 15 read as the scale times 2^-120
+// (subnormal scales too); a packed multiply by 2^120 makes it exact.
+__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t b) {
+  const uint32_t h = ((b & 0x7Fu) << 4) | ((b & 0x80u) << 8);
+  uint32_t v;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(h * 0x10001u), "r"(0x7B807B80u));   // 0x7B80 = bf16 2^120
+  return v;
+}
+
+// Dequantise chunk c (0..7) of a stage row in the weight format FMT; sw4: the row's 16 scale bytes of
+// the stage (int4: eight bf16 scales, one per chunk; fp4: sixteen E4M3 scales, two per chunk).
+template <int FMT>
+__device__ __forceinline__ void dequant_chunk(const uint4& wv, const uint32_t (&sw4)[4], int c, uint32_t* out16) {
+  if (FMT == WFMT_FP4) {
+    const uint32_t pair = (sw4[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu;   // scale bytes 2c, 2c + 1
+    dequant_group_fp4(wv, e4m3_to_bf16x2(pair & 0xFFu), e4m3_to_bf16x2(pair >> 8), out16);
+  } else {
+    dequant_group(wv, (c & 1) ? (sw4[c >> 1] >> 16) : (sw4[c >> 1] & 0xFFFFu), out16);
+  }
+}
+
 // A buffer b is reused every NB stages and the stages alternate between two dequant groups, so
 // its barriers are kept per (g % 2, b); the stages sharing one are P = lcm(2, NB) apart and g / P
 // counts the earlier ones. Buffer b is handed from stage g to stage g + NB: stage g waits for as
@@ -157,6 +203,16 @@ inline bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of a stage's scales: 64 rows x 16 bytes (int4: eight bf16 per row of the stage's 256
+// inputs; fp4: sixteen E4M3 bytes). K must be a multiple of 256 (16-byte row stride).
+inline bool make_scale_map(CUtensorMap* m, int wfmt, const void* scales, int K, int64_t rows_total) {
+  if (wfmt == WFMT_FP4)
+    return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, scales, K / 16, rows_total, K / 16, 16, 64,
+                       CU_TENSOR_MAP_SWIZZLE_NONE);
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, K / 32, rows_total, K / 16, 8, 64,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace tc

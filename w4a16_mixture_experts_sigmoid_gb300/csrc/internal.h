@@ -80,7 +80,12 @@ struct GemmProblem {
   float* partial = nullptr;  // fp32 [ksplit][R][2][out_cols] (gate/up) or [ksplit][R][out_cols]
   bool a_mma_order;        // rows of a are stored in MMA K order
   bool out_mma_order;      // gate/up: write h in MMA K order
+  int wfmt = 0;            // WFMT_INT4: int4 + bf16 scale per 32; WFMT_FP4: E2M1 + E4M3 scale per 16
+  const float* gscale = nullptr;   // WFMT_FP4: fp32 scale of each expert's matrix, [E]
 };
+
+// weight formats of the routed experts
+enum WeightFormat { WFMT_INT4 = 0, WFMT_FP4 = 1 };
 
 cudaError_t launch_gemm_simt(const GemmProblem& p, cudaStream_t s);
 

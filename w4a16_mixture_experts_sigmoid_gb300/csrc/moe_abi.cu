@@ -53,9 +53,9 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-moe_status_t check_dims(const moe_dims_t& d) {
+moe_status_t check_dims(const moe_dims_t& d, int fmt = WFMT_INT4) {
   if (d.E < 1 || d.E > 1024 || d.top_k < 1 || d.top_k > d.E) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (d.group != 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (d.group != (fmt == WFMT_FP4 ? 16 : 32)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (d.H < 32 || d.H % 32 || d.H > kMaxDim || d.I < 32 || d.I % 32 || d.I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
@@ -73,6 +73,44 @@ moe_status_t check_weights(const moe_weights_t* w, bool need_shared) {
     if (w->shared_I < 64 || w->shared_I % 64 || w->shared_I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
   }
   return MOE_OK;
+}
+
+moe_status_t check_weights_fp4(const moe_weights_fp4_t* w) {
+  if (w == nullptr || w->w13_packed == nullptr || w->w13_scale == nullptr || w->w13_gscale == nullptr ||
+      w->w2_packed == nullptr || w->w2_scale == nullptr || w->w2_gscale == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w13_packed) || !aligned16(w->w13_scale) || !aligned16(w->w2_packed) || !aligned16(w->w2_scale))
+    return MOE_ERR_INVALID_ARG;
+  const bool has_shared = w->shared_wgu != nullptr || w->shared_wd != nullptr || w->shared_I != 0;
+  if (has_shared) {
+    if (w->shared_wgu == nullptr || w->shared_wd == nullptr || !aligned16(w->shared_wgu) || !aligned16(w->shared_wd))
+      return MOE_ERR_INVALID_ARG;
+    if (w->shared_I < 64 || w->shared_I % 64 || w->shared_I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  return MOE_OK;
+}
+
+// One layer's weights as the kernels take them, in either routed-expert format.
+struct LayerW {
+  int fmt;
+  const int32_t* w13;
+  const void* s13;
+  const float* g13;
+  const int32_t* w2;
+  const void* s2;
+  const float* g2;
+  const uint16_t* sh_gu;
+  const uint16_t* sh_d;
+  int32_t shared_I;
+};
+
+LayerW layer_w(const moe_weights_t* w) {
+  return {WFMT_INT4, w->w13_packed, w->w13_scale, nullptr, w->w2_packed, w->w2_scale, nullptr,
+          w->shared_wgu, w->shared_wd, w->shared_I};
+}
+LayerW layer_w(const moe_weights_fp4_t* w) {
+  return {WFMT_FP4, w->w13_packed, w->w13_scale, w->w13_gscale, w->w2_packed, w->w2_scale, w->w2_gscale,
+          w->shared_wgu, w->shared_wd, w->shared_I};
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -144,7 +182,7 @@ int auto_tokens_per_tile(int64_t rows, int groups) {
 // the tensor-core K order. The tensor-core kernel needs its token rows in that
 // order; natural-order rows are first rewritten into `scratch` (R * K * 2 bytes).
 // out is bf16, or fp32 for the down projection with MOE_FLAG_OUT_F32.
-moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights_t* w, const uint16_t* a,
+moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, const uint16_t* a,
                               int32_t T, const int32_t* offsets, void* out, int* status, uint32_t flags,
                               bool rows_mma_order, uint16_t* scratch, int sms, cudaStream_t s) {
   GemmProblem p;
@@ -161,20 +199,26 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
   p.uniform_rows = -1;
   p.a_mma_order = rows_mma_order;
   p.out_mma_order = rows_mma_order;
+  p.wfmt = w.fmt;
   if (op == MOE_GEMM_GATEUP_SILU) {
-    p.w = w->w13_packed;
-    p.scales = w->w13_scale;
+    p.w = w.w13;
+    p.scales = static_cast<const uint16_t*>(w.s13);
+    p.gscale = w.g13;
     p.K = d.H;
     p.rows_per_expert = 2 * d.I;
     p.out_cols = d.I;
   } else {
-    p.w = w->w2_packed;
-    p.scales = w->w2_scale;
+    p.w = w.w2;
+    p.scales = static_cast<const uint16_t*>(w.s2);
+    p.gscale = w.g2;
     p.K = d.I;
     p.rows_per_expert = d.H;
     p.out_cols = d.H;
   }
-  if (flags & MOE_FLAG_GEMM_SIMT) return cuda_status(launch_gemm_simt(p, s));
+  if (flags & MOE_FLAG_GEMM_SIMT) {
+    if (w.fmt != WFMT_INT4) return MOE_ERR_UNSUPPORTED_SHAPE;   // the CUDA-core baseline reads int4 only
+    return cuda_status(launch_gemm_simt(p, s));
+  }
   const int asrc = (flags & MOE_FLAG_A_SMEM) ? A_SMEM_DQ : A_TMEM_DQ;
   int nt = static_cast<int>((flags >> 8) & 0xFFu);
   const bool auto_nt = nt == 0;
@@ -219,9 +263,9 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const moe_weights
 // than the SMs when a small batch fills one token tile; then each GEMM splits its K loop into
 // slices (fp32 partial sums in `part`, finished by a second kernel) so that every SM streams
 // weights. part may be null (no split). out is bf16, or fp32 with MOE_FLAG_OUT_F32.
-moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, int32_t T, uint16_t* hs,
+moe_status_t run_shared(const moe_dims_t& d, const LayerW& w, const uint16_t* x, int32_t T, uint16_t* hs,
                         void* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
-  const int Is = w->shared_I;
+  const int Is = w.shared_I;
   GemmProblem p;
   p.bf16_weights = true;
   p.scales = nullptr;
@@ -234,7 +278,7 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   p.out_mma_order = false;
   // gate/up: [T][H] -> hs [T][Is]
   p.op = MOE_GEMM_GATEUP_SILU;
-  p.w = w->shared_wgu;
+  p.w = w.sh_gu;
   p.a = x;
   p.out = hs;
   p.K = d.H;
@@ -251,7 +295,7 @@ moe_status_t run_shared(const moe_dims_t& d, const moe_weights_t* w, const uint1
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
   // down: hs [T][Is] -> out [T][H]
   p.op = MOE_GEMM_DOWN;
-  p.w = w->shared_wd;
+  p.w = w.sh_d;
   p.a = hs;
   const bool f32 = (flags & MOE_FLAG_OUT_F32) != 0;
   p.out = f32 ? nullptr : static_cast<uint16_t*>(out);
@@ -308,10 +352,10 @@ moe_status_t check_router(const uint16_t* x, const uint16_t* wg, int32_t T, int3
 }
 
 // One layer. residual (nullable, [T][H]) is added to the output in the combine's fp32 sum.
-moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const uint16_t* x, const float* logits,
+moe_status_t forward_device(const moe_dims_t& d, const LayerW& w, const uint16_t* x, const float* logits,
                             int32_t T, const uint16_t* residual, uint16_t* out, uint8_t* ws, uint32_t flags, int sms,
                             cudaStream_t s) {
-  const Layout L = layout(d, T, w->shared_I);
+  const Layout L = layout(d, T, w.shared_I);
   int* status = reinterpret_cast<int*>(ws);
   int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
   float* tw = reinterpret_cast<float*>(ws + L.w);
@@ -337,7 +381,7 @@ moe_status_t forward_device(const moe_dims_t& d, const moe_weights_t* w, const u
                         sms, s);
   if (st != MOE_OK) return st;
   const float* addend = nullptr;
-  if (w->shared_wgu != nullptr) {
+  if (w.sh_gu != nullptr) {
     uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
     float* ys = reinterpret_cast<float*>(ws + L.ys);
     float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
@@ -367,7 +411,8 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 size_t moe_workspace_size(moe_dims_t d, int32_t T, int32_t shared_I, uint32_t flags) {
-  if (check_dims(d) != MOE_OK || check_T(T, d.top_k) != MOE_OK || shared_I < 0) return 0;
+  if ((check_dims(d) != MOE_OK && check_dims(d, WFMT_FP4) != MOE_OK) || check_T(T, d.top_k) != MOE_OK || shared_I < 0)
+    return 0;
   return layout(d, T, shared_I, (flags & MOE_FLAG_ROUTER_PROJECT) != 0).end;
 }
 
@@ -483,7 +528,7 @@ moe_status_t moe_w4a16_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  return run_grouped_gemm(op, d, w, a_rows, T, expert_offsets, static_cast<void*>(out_rows), reinterpret_cast<int*>(w8),
+  return run_grouped_gemm(op, d, layer_w(w), a_rows, T, expert_offsets, static_cast<void*>(out_rows), reinterpret_cast<int*>(w8),
                           flags, rows_mma,
                           convert ? reinterpret_cast<uint16_t*>(w8 + 256) : nullptr, di.sms, as_stream(stream));
 }
@@ -506,7 +551,7 @@ moe_status_t moe_shared_expert(moe_dims_t d, const moe_weights_t* w, const uint1
   if ((st = current_device(&di)) != MOE_OK) return st;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(w8 + L.part) : nullptr;
-  return run_shared(d, w, x, T, reinterpret_cast<uint16_t*>(w8 + L.hs), out, reinterpret_cast<int*>(w8), flags,
+  return run_shared(d, layer_w(w), x, T, reinterpret_cast<uint16_t*>(w8 + L.hs), out, reinterpret_cast<int*>(w8), flags,
                     di.sms, part, as_stream(stream));
 }
 
@@ -551,7 +596,52 @@ moe_status_t moe_forward(moe_dims_t d, const moe_weights_t* w, const uint16_t* x
   if (ws_bytes < layout(d, T, w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
   DevInfo di;
   if ((st = current_device(&di)) != MOE_OK) return st;
-  return forward_device(d, w, x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
+  return forward_device(d, layer_w(w), x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
+                        as_stream(stream));
+}
+
+moe_status_t moe_fp4_grouped_gemm(int32_t op, moe_dims_t d, const moe_weights_fp4_t* w, const uint16_t* a_rows,
+                                  int32_t T, const int32_t* expert_offsets, uint16_t* out_rows, void* ws,
+                                  size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_fp4_grouped_gemm");
+  if (op != MOE_GEMM_GATEUP_SILU && op != MOE_GEMM_DOWN) return MOE_ERR_INVALID_ARG;
+  if (op == MOE_GEMM_GATEUP_SILU && (flags & MOE_FLAG_OUT_F32)) return MOE_ERR_INVALID_ARG;
+  if (flags & (MOE_FLAG_GEMM_SIMT | MOE_FLAG_A_SMEM)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t st = check_dims(d, WFMT_FP4);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights_fp4(w)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (a_rows == nullptr || expert_offsets == nullptr || out_rows == nullptr || ws == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a_rows) || !aligned16(out_rows) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  const bool rows_mma = (flags & MOE_FLAG_ROWS_MMA_ORDER) != 0;
+  const size_t K = (op == MOE_GEMM_GATEUP_SILU) ? d.H : d.I;
+  const size_t need = 256 + (rows_mma ? 0 : align256(static_cast<size_t>(T) * d.top_k * K * 2));
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  return run_grouped_gemm(op, d, layer_w(w), a_rows, T, expert_offsets, static_cast<void*>(out_rows),
+                          reinterpret_cast<int*>(w8), flags, rows_mma,
+                          rows_mma ? nullptr : reinterpret_cast<uint16_t*>(w8 + 256), di.sms, as_stream(stream));
+}
+
+moe_status_t moe_forward_fp4(moe_dims_t d, const moe_weights_fp4_t* w, const uint16_t* x, const float* logits,
+                             int32_t T, uint16_t* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_forward_fp4");
+  if (flags & (MOE_FLAG_GEMM_SIMT | MOE_FLAG_A_SMEM)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status_t st = check_dims(d, WFMT_FP4);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights_fp4(w)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || logits == nullptr || out == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout(d, T, w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  return forward_device(d, layer_w(w), x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
                         as_stream(stream));
 }
 
@@ -575,7 +665,7 @@ moe_status_t moe_forward_project(moe_dims_t d, const moe_weights_t* w, const uin
   cudaStream_t s = as_stream(stream);
   st = run_router(x, w_gate, T, d.E, d.H, logits, reinterpret_cast<int*>(w8), flags, di.sms, part, s);
   if (st != MOE_OK) return st;
-  return forward_device(d, w, x, logits, T, nullptr, out, w8, flags, di.sms, s);
+  return forward_device(d, layer_w(w), x, logits, T, nullptr, out, w8, flags, di.sms, s);
 }
 
 moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16_t* x_host, const float* logits_host,
@@ -601,7 +691,7 @@ moe_status_t moe_forward_host(moe_dims_t d, const moe_weights_t* w, const uint16
   cudaStream_t s = as_stream(stream);
   if (cudaMemcpyAsync(dx, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpyAsync(dl, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = forward_device(d, w, dx, dl, T, nullptr, dout, w8, flags, di.sms, s);
+  st = forward_device(d, layer_w(w), dx, dl, T, nullptr, dout, w8, flags, di.sms, s);
   if (st != MOE_OK) return st;
   return cuda_status(cudaMemcpyAsync(out_host, dout, xb, cudaMemcpyDeviceToHost, s));
 }
@@ -664,7 +754,7 @@ moe_status_t moe_stack_forward(moe_dims_t d, const moe_weights_t* layers, int32_
   for (int32_t l = 0; l < L; ++l) {
     uint16_t* next = (l == L - 1) ? out : ping[l & 1];
     if (launch_rmsnorm(cur, T, d.H, eps, xn, s) != cudaSuccess) return MOE_ERR_CUDA;
-    st = forward_device(d, &layers[l], xn, logits[l], T, cur, next, w8, flags, di.sms, s);
+    st = forward_device(d, layer_w(&layers[l]), xn, logits[l], T, cur, next, w8, flags, di.sms, s);
     if (st != MOE_OK) return st;
     cur = next;
   }

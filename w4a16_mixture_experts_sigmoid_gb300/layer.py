@@ -115,3 +115,61 @@ class MoeW4A16Stack:
 
     def check_status(self, stream=None) -> int:
         return 0 if self._ws is None else B.moe_check_status(self._ws, stream)
+
+
+class MoeFp4Layer:
+    """One routed-expert layer with 4-bit float weights (E2M1 codes, an E4M3 scale per 16 inputs,
+    an fp32 scale per matrix and expert; optional bf16 shared expert), resident on the GPU; every
+    call goes through the C ABI (moe_forward_fp4)."""
+
+    def __init__(self, E: int, top_k: int, H: int, I: int, w13, s13, g13, w2, s2, g2, shared_wgu=None,
+                 shared_wd=None, device="cuda"):
+        def dev(a, dtype):
+            if a is None:
+                return None
+            t = torch.as_tensor(a) if not isinstance(a, torch.Tensor) else a
+            return t.to(device=device, dtype=dtype).contiguous()
+
+        self.E, self.top_k, self.H, self.I = E, top_k, H, I
+        self.w13, self.s13, self.g13 = dev(w13, torch.int32), dev(s13, torch.uint8), dev(g13, torch.float32)
+        self.w2, self.s2, self.g2 = dev(w2, torch.int32), dev(s2, torch.uint8), dev(g2, torch.float32)
+        self.sh_gu = dev(shared_wgu, torch.int16)
+        self.sh_d = dev(shared_wd, torch.int16)
+        self.dims = B.dims(E, top_k, H, I, group=16)
+        self.weights = B.weights_fp4(self.w13, self.s13, self.g13, self.w2, self.s2, self.g2, self.sh_gu, self.sh_d)
+        self.shared_I = 0 if self.sh_d is None else int(self.sh_d.shape[1])
+        self._ws = None
+        self.device = device
+
+    @classmethod
+    def from_arrays(cls, shape, arrays: dict, device="cuda"):
+        import numpy as np
+
+        def t(key):
+            a = arrays.get(key)
+            if a is None:
+                return None
+            a = np.ascontiguousarray(a)
+            if a.dtype == np.uint16:
+                a = a.view(np.int16)
+            return torch.from_numpy(a)
+
+        return cls(shape.E, shape.top_k, shape.H, shape.I, t("w13"), t("s13"), t("g13"), t("w2"), t("s2"), t("g2"),
+                   t("sh_gu"), t("sh_d"), device=device)
+
+    def workspace(self, T: int) -> torch.Tensor:
+        need = B.moe_workspace_size(self.dims, T, self.shared_I)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.zeros(need, dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, out: torch.Tensor | None = None, flags: int = 0,
+                stream=None) -> torch.Tensor:
+        T = int(x.shape[0])
+        if out is None:
+            out = torch.empty((T, self.H), dtype=torch.int16, device=self.device)
+        B.moe_forward_fp4(self.dims, self.weights, x, logits, T, out, self.workspace(T), flags, stream)
+        return out
+
+    def check_status(self, stream=None) -> int:
+        return 0 if self._ws is None else B.moe_check_status(self._ws, stream)
