@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   if (warp == 0) {
     // ------------------------------------------------------------ weight producer (this CTA's rows)
     const uint64_t pol_w = l2_policy_evict_first();
+    constexpr int kScaleX = scale_x_per_stage<FMT>();   // one stage of scales, in map elements (16 bytes)
     const uint32_t txw = C::kAStage + (p.scale_tma ? BM * 16 : 0);
     const int kg = p.K / 32;
     int g = 0;
@@ -210,8 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           tma_load_2d(sa, &p.tm_w, wf, ks * (BK / 8), grow_lo, pol_w);
           tma_load_2d(sa + 64 * 128, &p.tm_w, wf, ks * (BK / 8), grow_hi, pol_w);
           if (p.scale_tma) {
-            tma_load_2d(ss, &p.tm_s, wf, ks * 8, grow_lo, pol_w);
-            tma_load_2d(ss + 64 * 16, &p.tm_s, wf, ks * 8, grow_hi, pol_w);
+            tma_load_2d(ss, &p.tm_s, wf, ks * kScaleX, grow_lo, pol_w);
+            tma_load_2d(ss + 64 * 16, &p.tm_s, wf, ks * kScaleX, grow_hi, pol_w);
           }
         } else {
           mbar_arrive(wf);

@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol_w = l2_policy_evict_first();
+    constexpr int kScaleX = scale_x_per_stage<FMT>();   // one stage of scales, in map elements (16 bytes)
     const uint32_t txw = C::kAStage + ((C::kDq && p.scale_tma) ? BM * 16 : 0);
     const int kg = p.K / 32;
     int g = 0;
@@ -280,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             tma_load_2d(sa, &p.tm_w, wf, (kb + ks) * (BK / 8), grow_lo, pol_w);
             tma_load_2d(sa + 64 * 128, &p.tm_w, wf, (kb + ks) * (BK / 8), grow_hi, pol_w);
             if (p.scale_tma) {
-              tma_load_2d(ss, &p.tm_s, wf, (kb + ks) * 8, grow_lo, pol_w);
-              tma_load_2d(ss + 64 * 16, &p.tm_s, wf, (kb + ks) * 8, grow_hi, pol_w);
+              tma_load_2d(ss, &p.tm_s, wf, (kb + ks) * kScaleX, grow_lo, pol_w);
+              tma_load_2d(ss + 64 * 16, &p.tm_s, wf, (kb + ks) * kScaleX, grow_hi, pol_w);
             }
           }
         } else {

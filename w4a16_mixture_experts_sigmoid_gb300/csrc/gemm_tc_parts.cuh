@@ -205,6 +205,12 @@ inline bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// x coordinate, in elements of the scale tensor map, of stage ks's scales: a stage's 16 bytes of a row are
+// eight bf16 (int4) or sixteen E4M3 bytes (fp4). A TMA load must start on a 16-byte boundary, which this
+// keeps for every stage.
+template <int FMT>
+__host__ __device__ constexpr int scale_x_per_stage() { return FMT == WFMT_FP4 ? 16 : 8; }
+
 // Tensor map of a stage's scales: 64 rows x 16 bytes (int4: eight bf16 per row of the stage's 256
 // inputs; fp4: sixteen E4M3 bytes). K must be a multiple of 256 (16-byte row stride).
 inline bool make_scale_map(CUtensorMap* m, int wfmt, const void* scales, int K, int64_t rows_total) {
