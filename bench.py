@@ -57,6 +57,9 @@ WORKLOADS = {
     # the same decode layer with 4-bit float weights: E2M1 codes, an E4M3 scale per 16 inputs, an fp32
     # scale per matrix and expert (the same 24.77 MB per expert)
     "decode_t64_nvfp4": dict(shape=synth.FULL, T=64, skew=None, fmt="nvfp4"),
+    # the decode layer with its routed bank in pinned host memory: each step copies the touched experts
+    # over the host link into a device bank, then runs the layer there
+    "decode_t64_offload": dict(shape=synth.FULL, T=64, skew=None, offload=True),
     "prefill_t4096_zipf_nvfp4": dict(shape=synth.FULL, T=4096, skew=1.1, fmt="nvfp4"),
 }
 
@@ -714,6 +717,151 @@ def run_stack(args):
         torch.distributed.destroy_process_group()
 
 
+def run_offload(args):
+    """The routed bank in host memory: one step = moe_forward_offload (route, permute, copy the touched
+    experts host -> device, GEMMs, combine). Bound by the host link's read rate, measured in this run."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    s = w["shape"]
+    T = w["T"]
+    arrays, x, logits = make_inputs(w, seed=0)
+    ht = {}
+    for k in ("w13", "s13", "w2", "s2"):
+        a = np.ascontiguousarray(arrays[k])
+        ht[k] = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+    del arrays
+    dt = {k: torch.empty_like(v, device=dev) for k, v in ht.items()}
+    hw = B.host_weights(ht["w13"], ht["s13"], ht["w2"], ht["s2"])
+    dw = B.weights(dt["w13"], dt["s13"], dt["w2"], dt["s2"])
+    dims = B.dims(s.E, s.top_k, s.H, s.I)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev)
+    ld = torch.from_numpy(logits).to(dev)
+    out = torch.empty((T, s.H), dtype=torch.int16, device=dev)
+    ws = torch.zeros(B.moe_workspace_size(dims, T), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.moe_forward_offload(dims, hw, dw, xd, ld, T, out, ws, args.flags)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if B.moe_check_status(ws) != 0:
+        raise RuntimeError("device status after warm-up")
+    # routing of the batch: which experts are touched
+    R = T * s.top_k
+    d_ids = torch.empty((T, s.top_k), dtype=torch.int32, device=dev)
+    d_w = torch.empty((T, s.top_k), dtype=torch.float32, device=dev)
+    d_off = torch.empty(s.E + 1, dtype=torch.int32, device=dev)
+    d_srt = torch.empty(R, dtype=torch.int32, device=dev)
+    d_inv = torch.empty(R, dtype=torch.int32, device=dev)
+    B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
+    B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, None, 0, None, ws)
+    torch.cuda.synchronize(dev)
+    touched = int((np.diff(d_off.cpu().numpy()) > 0).sum())
+    gu_b, dn_b = expert_bytes(s)
+
+    clocks = ClockSampler(None)
+    clocks.start()
+    torch.cuda.synchronize(dev)
+    n0 = B.moe_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = B.moe_launch_count() - n0
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(ms, dev)
+    if B.moe_check_status(ws) != 0:
+        raise RuntimeError("device status after the timed region")
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    # the staging kernel alone on this batch's experts, and on every expert of the bank
+    stage_ms = timed(lambda: B.moe_stage_experts(dims, hw, d_off, dw))
+    all_off = torch.arange(s.E + 1, dtype=torch.int32, device=dev)
+    stage_all_ms = timed(lambda: B.moe_stage_experts(dims, hw, all_off, dw), reps=3)
+    # the host link's read rate through the copy engines: 4 GiB of pinned host memory -> device
+    hbuf = torch.empty(1 << 32, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(1 << 32, dtype=torch.uint8, device=dev)
+    h2d_ms = timed(lambda: dbuf.copy_(hbuf, non_blocking=True), reps=3)
+    h2d_gbs = (1 << 32) / (h2d_ms * 1e-3) / 1e9
+    del hbuf, dbuf
+    bank_bytes = s.E * (gu_b + dn_b)
+    stage_bytes = touched * (gu_b + dn_b)
+    stage_gbs = stage_bytes / (stage_ms * 1e-3) / 1e9
+    stage_all_gbs = bank_bytes / (stage_all_ms * 1e-3) / 1e9
+    link_peak = max(h2d_gbs, stage_all_gbs)
+    roofline = {"bound": "host-link", "achieved": stage_gbs, "peak": link_peak, "unit": "GB/s",
+                "frac": stage_gbs / link_peak, "traffic": None, "kernel": "stage_experts", "kernel_ms": stage_ms,
+                "algorithmic_bytes_per_launch": stage_bytes,
+                "peak_source": (f"measured in this run: the larger of a 4 GiB pinned host->device copy "
+                                f"({h2d_gbs:.1f} GB/s) and the staging kernel over the whole bank "
+                                f"({stage_all_gbs:.1f} GB/s); MEASURED_PEAKS.json has no host-link figure")}
+    step_roof_ms = stage_bytes / (link_peak * 1e9) * 1e3
+    value = whole_job_tokens_per_s(T, world, ms_max * 1e-3)
+    # end to end: pinned host x and logits in, host result out
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    lh = torch.from_numpy(logits).pin_memory()
+    oh = torch.empty((T, s.H), dtype=torch.int16).pin_memory()
+    xe, le = torch.empty_like(xd), torch.empty_like(ld)
+
+    def e2e_step():
+        xe.copy_(xh, non_blocking=True)
+        le.copy_(lh, non_blocking=True)
+        B.moe_forward_offload(dims, hw, dw, xe, le, T, out, ws, args.flags)
+        oh.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    e2e_step()
+    esteps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(esteps):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / esteps, dev)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(args.workload, w) + ", routed bank in pinned host memory",
+                   "T": T, "E": s.E, "top_k": s.top_k, "H": s.H, "I": s.I, "parallelism": f"replicas x{world}",
+                   "l2": f"no flush: each step copies {touched} experts ({stage_bytes / 1e9:.2f} GB) from host "
+                         f"memory", "flags": args.flags},
+        "roofline": roofline,
+        "step_roofline": {"touched_experts": touched, "bytes_over_host_link": stage_bytes,
+                          "roofline_ms": step_roof_ms, "frac": step_roof_ms / ms,
+                          "stage_ms": stage_ms, "stage_all_experts_ms": stage_all_ms, "h2d_copy_gbs": h2d_gbs},
+        "cpu_baseline": None,
+        "e2e": {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.nbytes + logits.nbytes, "d2h_bytes_per_step": T * s.H * 2,
+                "ms_per_step": e2e_s * 1e3},
+        "gpu_launches": launches, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -730,6 +878,8 @@ def main():
         run_reference(args)
     elif WORKLOADS[args.workload].get("layers", 1) > 1:
         run_stack(args)
+    elif WORKLOADS[args.workload].get("offload"):
+        run_offload(args)
     else:
         run_ours(args)
 

@@ -344,6 +344,29 @@ MOE_API moe_status_t moe_forward_fp4(moe_dims_t d, const moe_weights_fp4_t* w, c
                              const float* logits, int32_t T, uint16_t* out, void* ws, size_t ws_bytes,
                              uint32_t flags, void* stream);
 
+/* The routed-expert bank in host memory. Passage: "Kimi-K2.6" catalog page,
+ * the paragraph on running with expert offload (8 of 384 experts per token:
+ * a token's expert traffic is a small slice of the checkpoint, so the bank can
+ * sit in system RAM).
+ * moe_stage_experts copies, for every expert e with rows (expert_offsets[e+1]
+ * > expert_offsets[e]), its W13, W13 scales, W2 and W2 scales from host_w to
+ * the same places of dev_w; other experts' places in dev_w are left as they
+ * are. host_w's four routed tensors must be page-locked host memory mapped
+ * into the device's address space (cudaHostAlloc, or pinned memory on a
+ * unified-addressing system): the GPU reads them over the host link
+ * (NVLink-C2C on a Grace-Blackwell node). Otherwise MOE_ERR_INVALID_ARG is
+ * returned before anything is launched. host_w's shared-expert pointers are
+ * not read. dev_w: a device bank of the full bank's layout (a layer's worth
+ * of device memory, reusable for every layer of a model).
+ * moe_forward_offload is moe_forward with the bank in host memory: route,
+ * permute, stage the touched experts into dev_w, then the GEMMs read dev_w
+ * (dev_w's bf16 shared expert, if any, stays resident). */
+MOE_API moe_status_t moe_stage_experts(moe_dims_t d, const moe_weights_t* host_w, const int32_t* expert_offsets,
+                               const moe_weights_t* dev_w, void* stream);
+MOE_API moe_status_t moe_forward_offload(moe_dims_t d, const moe_weights_t* host_w, const moe_weights_t* dev_w,
+                                 const uint16_t* x, const float* logits, int32_t T, uint16_t* out, void* ws,
+                                 size_t ws_bytes, uint32_t flags, void* stream);
+
 /* The whole layer from the token activations alone: the router logits are
  * projected from x with w_gate (bf16 [E][H], as moe_router_logits) into the
  * workspace, then the layer runs as moe_forward on them.

@@ -70,6 +70,9 @@ SIGNATURES = {
                                        c_void_p, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_forward_fp4": (c_int32, [moe_dims_t, POINTER(moe_weights_fp4_t), c_void_p, c_void_p, c_int32, c_void_p,
                                   c_void_p, c_size_t, c_uint32, c_void_p]),
+    "moe_stage_experts": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, POINTER(moe_weights_t), c_void_p]),
+    "moe_forward_offload": (c_int32, [moe_dims_t, POINTER(moe_weights_t), POINTER(moe_weights_t), c_void_p, c_void_p,
+                                      c_int32, c_void_p, c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_forward_project": (c_int32, [moe_dims_t, POINTER(moe_weights_t), c_void_p, c_void_p, c_int32, c_void_p,
                                       c_void_p, c_size_t, c_uint32, c_void_p]),
     "moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
@@ -205,6 +208,28 @@ def moe_route_project(x, w_gate, T: int, E: int, H: int, k: int, logits, topk_id
     _check(load().moe_route_project(_dptr(x), _dptr(w_gate), T, E, H, k, _dptr(logits), _dptr(topk_ids),
                                     _dptr(topk_w), _dptr(ws), _nbytes(ws), flags, _stream(stream)),
            "moe_route_project")
+
+
+def host_weights(w13, s13, w2, s2) -> moe_weights_t:
+    """moe_weights_t of a routed bank in page-locked host memory (pinned CPU tensors): the library
+    reads it over the host link (moe_stage_experts, moe_forward_offload)."""
+    for t in (w13, s13, w2, s2):
+        if t.is_cuda or not t.is_pinned():
+            raise ValueError("a host bank is made of pinned CPU tensors")
+    return moe_weights_t(_ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), None, None, 0)
+
+
+def moe_stage_experts(d: moe_dims_t, host_w: moe_weights_t, expert_offsets, dev_w: moe_weights_t,
+                      stream=None) -> None:
+    _check(load().moe_stage_experts(d, ctypes.byref(host_w), _dptr(expert_offsets), ctypes.byref(dev_w),
+                                    _stream(stream)), "moe_stage_experts")
+
+
+def moe_forward_offload(d: moe_dims_t, host_w: moe_weights_t, dev_w: moe_weights_t, x, logits, T: int, out, ws,
+                        flags: int = 0, stream=None) -> None:
+    _check(load().moe_forward_offload(d, ctypes.byref(host_w), ctypes.byref(dev_w), _dptr(x), _dptr(logits), T,
+                                      _dptr(out), _dptr(ws), _nbytes(ws), flags, _stream(stream)),
+           "moe_forward_offload")
 
 
 def weights_fp4(w13, s13, g13, w2, s2, g2, sh_gu=None, sh_d=None) -> moe_weights_fp4_t:

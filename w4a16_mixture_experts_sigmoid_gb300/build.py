@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w4a16.so")
 SOURCES = ["moe_abi.cu", "route.cu", "permute.cu", "permute_static.cu", "combine.cu", "stack.cu", "gemm_simt.cu",
-           "gemm_tc.cu", "gemm_pair.cu"]
+           "gemm_tc.cu", "gemm_pair.cu", "offload.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          f"-I{os.path.join(ROOT, 'include')}"]

@@ -97,6 +97,11 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int tokens_per_tile, 
 // cta_group::2 MMA covers 256 weight rows over two SMs; nt in {16, 32, 64, 128}
 cudaError_t launch_gemm_pair(const GemmProblem& p, int tokens_per_tile, int num_sms, cudaStream_t s);
 
+// copy every expert with rows (offsets) of the four bank tensors from the host bank (device-accessible
+// addresses of page-locked host memory) into the device bank of the same layout; bytes: per expert
+cudaError_t launch_stage_experts(const void* const host_dev[4], void* const dev[4], const int64_t bytes[4],
+                                 const int32_t* offsets, int E, cudaStream_t s);
+
 cudaError_t launch_expire_wait(int* status, int64_t timeout_ns, cudaStream_t s);
 
 }  // namespace moe

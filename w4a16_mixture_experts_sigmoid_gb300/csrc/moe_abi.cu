@@ -351,10 +351,49 @@ moe_status_t check_router(const uint16_t* x, const uint16_t* wg, int32_t T, int3
   return MOE_OK;
 }
 
+// A host bank staged into the device bank before the GEMMs (moe_forward_offload).
+struct Staging {
+  const void* src[4];   // device-accessible addresses of the host bank's w13, s13, w2, s2
+  void* dst[4];         // the device bank's
+  int64_t bytes[4];     // per expert
+};
+
+int64_t bank_bytes_per_expert(const moe_dims_t& d, int i) {
+  const int64_t H = d.H, I = d.I;
+  switch (i) {
+    case 0: return 2 * I * (H / 8) * 4;
+    case 1: return 2 * I * (H / 32) * 2;
+    case 2: return H * (I / 8) * 4;
+    default: return H * (I / 32) * 2;
+  }
+}
+
+// Device-accessible addresses of a host bank: each tensor must be page-locked host memory mapped
+// into the device's address space (cudaHostAlloc / pinned memory on a unified-addressing system).
+// An error the caller left pending stays as it was.
+moe_status_t host_bank(const moe_dims_t& d, const moe_weights_t* hw, const moe_weights_t* dw, Staging* st) {
+  const void* h[4] = {hw->w13_packed, hw->w13_scale, hw->w2_packed, hw->w2_scale};
+  void* dv[4] = {const_cast<int32_t*>(dw->w13_packed), const_cast<uint16_t*>(dw->w13_scale),
+                 const_cast<int32_t*>(dw->w2_packed), const_cast<uint16_t*>(dw->w2_scale)};
+  const cudaError_t pending = cudaPeekAtLastError();
+  for (int i = 0; i < 4; ++i) {
+    void* p = nullptr;
+    if (cudaHostGetDevicePointer(&p, const_cast<void*>(h[i]), 0) != cudaSuccess || p == nullptr ||
+        !aligned16(p)) {
+      if (pending == cudaSuccess) (void)cudaGetLastError();
+      return MOE_ERR_INVALID_ARG;
+    }
+    st->src[i] = p;
+    st->dst[i] = dv[i];
+    st->bytes[i] = bank_bytes_per_expert(d, i);
+  }
+  return MOE_OK;
+}
+
 // One layer. residual (nullable, [T][H]) is added to the output in the combine's fp32 sum.
 moe_status_t forward_device(const moe_dims_t& d, const LayerW& w, const uint16_t* x, const float* logits,
                             int32_t T, const uint16_t* residual, uint16_t* out, uint8_t* ws, uint32_t flags, int sms,
-                            cudaStream_t s) {
+                            cudaStream_t s, const Staging* stage = nullptr) {
   const Layout L = layout(d, T, w.shared_I);
   int* status = reinterpret_cast<int*>(ws);
   int32_t* ids = reinterpret_cast<int32_t*>(ws + L.ids);
@@ -372,6 +411,8 @@ moe_status_t forward_device(const moe_dims_t& d, const LayerW& w, const uint16_t
   cudaError_t e = launch_route(logits, T, d.E, d.top_k, ids, tw, s);
   if (e == cudaSuccess) e = launch_permute(ids, T, d.E, d.top_k, offsets, sorted, inv, hist, status, s);
   if (e == cudaSuccess) e = launch_gather(x, sorted, offsets, d.E, R, d.H, mma_order, xperm, s);
+  if (e == cudaSuccess && stage != nullptr)   // the touched experts, host bank -> device bank
+    e = launch_stage_experts(stage->src, stage->dst, stage->bytes, offsets, d.E, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, mma_order,
                                      nullptr, sms, s);
@@ -643,6 +684,42 @@ moe_status_t moe_forward_fp4(moe_dims_t d, const moe_weights_fp4_t* w, const uin
   if ((st = current_device(&di)) != MOE_OK) return st;
   return forward_device(d, layer_w(w), x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
                         as_stream(stream));
+}
+
+moe_status_t moe_stage_experts(moe_dims_t d, const moe_weights_t* host_w, const int32_t* expert_offsets,
+                               const moe_weights_t* dev_w, void* stream) {
+  CallRange range_("moe_stage_experts");
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_weights(host_w, false)) != MOE_OK) return st;
+  if ((st = check_weights(dev_w, false)) != MOE_OK) return st;
+  if (expert_offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  Staging sg;
+  if ((st = host_bank(d, host_w, dev_w, &sg)) != MOE_OK) return st;
+  return cuda_status(launch_stage_experts(sg.src, sg.dst, sg.bytes, expert_offsets, d.E, as_stream(stream)));
+}
+
+moe_status_t moe_forward_offload(moe_dims_t d, const moe_weights_t* host_w, const moe_weights_t* dev_w,
+                                 const uint16_t* x, const float* logits, int32_t T, uint16_t* out, void* ws,
+                                 size_t ws_bytes, uint32_t flags, void* stream) {
+  CallRange range_("moe_forward_offload");
+  moe_status_t st = check_dims(d);
+  if (st != MOE_OK) return st;
+  if ((st = check_T(T, d.top_k)) != MOE_OK) return st;
+  if ((st = check_weights(host_w, false)) != MOE_OK) return st;
+  if ((st = check_weights(dev_w, false)) != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (x == nullptr || logits == nullptr || out == nullptr || ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < layout(d, T, dev_w->shared_I).end) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo di;
+  if ((st = current_device(&di)) != MOE_OK) return st;
+  Staging sg;
+  if ((st = host_bank(d, host_w, dev_w, &sg)) != MOE_OK) return st;
+  return forward_device(d, layer_w(dev_w), x, logits, T, nullptr, out, static_cast<uint8_t*>(ws), flags, di.sms,
+                        as_stream(stream), &sg);
 }
 
 moe_status_t moe_forward_project(moe_dims_t d, const moe_weights_t* w, const uint16_t* w_gate, const uint16_t* x,
