@@ -34,6 +34,29 @@ def test_sigmoid_bit_identical_on_a_strided_sweep_of_all_fp32(cuda_lib):
         assert bad.size == 0, f"{bad.size} mismatches, first x={x[bad[:5]]} gpu={g[bad[:5]]} cpu={r[bad[:5]]}"
 
 
+@pytest.mark.slow
+def test_sigmoid_bit_identical_on_every_fp32(cuda_lib):
+    """All 2^32 bit patterns, in 128 chunks of 2^25: the GPU's score of each equals the oracle's,
+    bit for bit (NaN inputs give NaN on both sides). The oracle's chunks run on a few host threads."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    n = 1 << 25
+
+    def cpu(c):
+        x = (np.arange(n, dtype=np.uint64) + np.uint64(c * n)).astype(np.uint32).view(np.float32)
+        return oracle.sigmoid_def(x)
+
+    with ThreadPoolExecutor(max(1, min(4, os.cpu_count() or 1))) as ex:
+        refs = ex.map(cpu, range(128))
+        for c, r in enumerate(refs):
+            x = (np.arange(n, dtype=np.uint64) + np.uint64(c * n)).astype(np.uint32).view(np.float32)
+            g = gpu_scores(B, x)
+            same = (g.view(np.uint32) == r.view(np.uint32)) | (np.isnan(g) & np.isnan(r))
+            bad = np.flatnonzero(~same)
+            assert bad.size == 0, f"chunk {c}: {bad.size} mismatches, first x={x[bad[:5]]} gpu={g[bad[:5]]}"
+
+
 def check_route(B, logits: np.ndarray, k: int):
     import torch
     T, E = logits.shape

@@ -89,10 +89,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   int16_t* act_e = reinterpret_cast<int16_t*>(tmem_slot + 4);
   int* tpre = reinterpret_cast<int*>(act_e + kMaxE);
 
-  // The successor in the stream may launch now: its CTAs take SMs as this grid's CTAs leave, and
-  // only its token-row producer waits for this grid to finish (griddep_wait below). The tile
-  // table and the weight stream read nothing the predecessor writes: the expert offsets come
-  // from the permutation, which finished before the predecessor could start.
+  // The successor in the stream may launch now: its CTAs take SMs as this grid's CTAs leave. The
+  // token-row producer always waits for the predecessor grid to finish (griddep_wait below). With
+  // weights_ready the tile table and the weight stream need not: the launcher guarantees that the
+  // weights and the expert offsets were complete before the kernels queued ahead of this one began
+  // (within one layer the offsets come from the permutation, finished before the predecessor could
+  // start); otherwise warp 0 waits too.
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair's MMAs; 1: its partner
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, C::kTmemCols);
   if (warp == 0) {
+    if (!p.weights_ready) griddep_wait();
     // compact list of experts with rows, and the prefix of their tile counts (both CTAs build the
     // same list from the same offsets)
     int cnts[kMaxE / 32];
@@ -568,6 +571,7 @@ cudaError_t launch_gemm_pair(const GemmProblem& p, int nt, int num_sms, cudaStre
   prm.uniform_rows = p.uniform_rows;
   prm.min_rows = p.min_rows;
   prm.max_rows = p.max_rows;
+  prm.weights_ready = p.weights_ready ? 1 : 0;
   prm.ksplit = 1;
   prm.partial = nullptr;
   prm.rows_total = static_cast<int>(rows_total);

@@ -134,10 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   int16_t* act_e = reinterpret_cast<int16_t*>(tmem_slot + 4);
   int* tpre = reinterpret_cast<int*>(act_e + kMaxE);
 
-  // The successor in the stream may launch now: its CTAs take SMs as this grid's CTAs leave, and
-  // only its token-row producer waits for this grid to finish (griddep_wait below). The tile
-  // table and the weight stream read nothing the predecessor writes: the expert offsets come
-  // from the permutation, which finished before the predecessor could start.
+  // The successor in the stream may launch now: its CTAs take SMs as this grid's CTAs leave. The
+  // token-row producer always waits for the predecessor grid to finish (griddep_wait below). With
+  // weights_ready the tile table and the weight stream need not: the launcher guarantees that the
+  // weights and the expert offsets were complete before the kernels queued ahead of this one began
+  // (within one layer the offsets come from the permutation, finished before the predecessor could
+  // start); otherwise warp 0 waits too.
   griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_wt = (OP == MOE_GEMM_GATEUP_SILU) ? (p.out_cols + 63) / 64 : (p.rows_per_expert + BM - 1) / BM;
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   if (warp == 0) {
+    if (!p.weights_ready) griddep_wait();
     // compact list of experts with rows, and the prefix of their tile counts
     if (p.uniform_rows >= 0) {
       if (lane == 0) {
@@ -705,6 +708,7 @@ cudaError_t launch_gemm_tc(const GemmProblem& p, int asrc, int nt, int num_sms, 
   prm.uniform_rows = p.uniform_rows;
   prm.min_rows = p.min_rows;
   prm.max_rows = p.max_rows;
+  prm.weights_ready = p.weights_ready ? 1 : 0;
   prm.ksplit = p.ksplit;
   prm.partial = p.partial;
   if (p.ksplit < 1 || ((p.K + BK - 1) / BK) % p.ksplit != 0 || (p.ksplit > 1 && p.partial == nullptr) ||

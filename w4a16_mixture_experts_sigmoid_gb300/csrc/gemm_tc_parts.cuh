@@ -39,6 +39,7 @@ struct TcParams {
   int* status;
   int E, K, rows_per_expert, out_cols, uniform_rows, scale_tma, rows_total, R, out_mma_order;
   int min_rows, max_rows;  // experts outside [min_rows, max_rows] rows are left to another launch
+  int weights_ready;       // 0: the tile table and the weight stream wait for the predecessor grid
   int ksplit;              // K slices per tile (1: whole K); > 1 (bf16 weights only) writes fp32 partial sums
   float* partial;          // [ksplit][R][2][I] (gate/up) or [ksplit][R][H] (down), when ksplit > 1
   unsigned long long timeout_ns;

@@ -81,6 +81,10 @@ struct GemmProblem {
   bool a_mma_order;        // rows of a are stored in MMA K order
   bool out_mma_order;      // gate/up: write h in MMA K order
   int wfmt = 0;            // WFMT_INT4: int4 + bf16 scale per 32; WFMT_FP4: E2M1 + E4M3 scale per 16
+  // The weights (and offsets) were complete before the calls queued ahead of this launch began:
+  // the kernel may then stream weights while its predecessor in the stream finishes. Otherwise
+  // (weights written by the previous kernel, or by a caller's kernel we cannot see) it waits first.
+  bool weights_ready = false;
   const float* gscale = nullptr;   // WFMT_FP4: fp32 scale of each expert's matrix, [E]
 };
 

@@ -184,8 +184,10 @@ int auto_tokens_per_tile(int64_t rows, int groups) {
 // out is bf16, or fp32 for the down projection with MOE_FLAG_OUT_F32.
 moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, const uint16_t* a,
                               int32_t T, const int32_t* offsets, void* out, int* status, uint32_t flags,
-                              bool rows_mma_order, uint16_t* scratch, int sms, cudaStream_t s) {
+                              bool rows_mma_order, uint16_t* scratch, int sms, cudaStream_t s,
+                              bool weights_ready = false) {
   GemmProblem p;
+  p.weights_ready = weights_ready;
   p.op = op;
   p.bf16_weights = false;
   p.a = a;
@@ -264,9 +266,11 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, 
 // slices (fp32 partial sums in `part`, finished by a second kernel) so that every SM streams
 // weights. part may be null (no split). out is bf16, or fp32 with MOE_FLAG_OUT_F32.
 moe_status_t run_shared(const moe_dims_t& d, const LayerW& w, const uint16_t* x, int32_t T, uint16_t* hs,
-                        void* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
+                        void* out, int* status, uint32_t flags, int sms, float* part, cudaStream_t s,
+                        bool weights_ready = false) {
   const int Is = w.shared_I;
   GemmProblem p;
+  p.weights_ready = weights_ready;
   p.bf16_weights = true;
   p.scales = nullptr;
   p.offsets = nullptr;
@@ -314,7 +318,7 @@ moe_status_t run_shared(const moe_dims_t& d, const LayerW& w, const uint16_t* x,
 // fp32 rows out. Small batches split K as the shared expert does (part may be null: no split).
 moe_status_t run_router(const uint16_t* x, const uint16_t* wg, int32_t T, int32_t E, int32_t H, float* logits,
                         int* status, uint32_t flags, int sms, float* part, cudaStream_t s) {
-  GemmProblem p;
+  GemmProblem p;   // weights_ready stays false: the gate matrix is the caller's, the first read of the call
   p.op = MOE_GEMM_DOWN;
   p.bf16_weights = true;
   p.w = wg;
@@ -414,19 +418,22 @@ moe_status_t forward_device(const moe_dims_t& d, const LayerW& w, const uint16_t
   if (e == cudaSuccess && stage != nullptr)   // the touched experts, host bank -> device bank
     e = launch_stage_experts(stage->src, stage->dst, stage->bytes, offsets, d.E, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // The layer's kernels before the GEMMs began with route's wait, so a resident bank and the offsets
+  // are complete when the GEMMs start; a bank staged by this call is not (it is the predecessor's output).
+  const bool ready = stage == nullptr;
   moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, mma_order,
-                                     nullptr, sms, s);
+                                     nullptr, sms, s, ready);
   if (st != MOE_OK) return st;
   // y (and the shared expert's output) stay fp32 until the combine's one bf16 rounding
   st = run_grouped_gemm(MOE_GEMM_DOWN, d, w, h, T, offsets, y, status, flags | MOE_FLAG_OUT_F32, mma_order, nullptr,
-                        sms, s);
+                        sms, s, ready);
   if (st != MOE_OK) return st;
   const float* addend = nullptr;
   if (w.sh_gu != nullptr) {
     uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
     float* ys = reinterpret_cast<float*>(ws + L.ys);
     float* part = L.part_bytes > 0 ? reinterpret_cast<float*>(ws + L.part) : nullptr;
-    st = run_shared(d, w, x, T, hs, ys, status, flags | MOE_FLAG_OUT_F32, sms, part, s);
+    st = run_shared(d, w, x, T, hs, ys, status, flags | MOE_FLAG_OUT_F32, sms, part, s, true);
     if (st != MOE_OK) return st;
     addend = ys;
   }
