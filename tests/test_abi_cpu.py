@@ -104,6 +104,13 @@ def test_arguments_rejected_before_any_launch(lib):
     assert L.moe_route_project(16, 16, 4, 384, 7168, 400, 16, 16, 16, 16, 1 << 20, 0, None) == \
         B.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_router_workspace_size(64, 384, 7168) > L.moe_router_workspace_size(512, 384, 7168) > 0
+    # offloaded bank: null tensors and a missing offsets array are refused before anything else
+    hw = B.moe_weights_t(None, None, None, None, None, None, 0)
+    dw = B.moe_weights_t(16, 16, 16, 16, None, None, 0)
+    assert L.moe_stage_experts(B.dims(8, 2, 256, 128), byref(hw), 16, byref(dw), None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_stage_experts(B.dims(8, 2, 256, 128), byref(dw), None, byref(dw), None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_offload(B.dims(8, 2, 256, 128), byref(dw), byref(hw), 16, 16, 4, 16, 16, 1 << 20, 0,
+                                 None) == B.MOE_ERR_INVALID_ARG
     d2 = B.dims(384, 8, 7168, 2048)
     assert L.moe_workspace_size(d2, 64, 0, B.MOE_FLAG_ROUTER_PROJECT) > L.moe_workspace_size(d2, 64, 0, 0)
     assert L.moe_check_status(None, None) == B.MOE_ERR_INVALID_ARG
