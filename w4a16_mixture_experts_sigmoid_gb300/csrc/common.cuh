@@ -274,9 +274,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared).
+// Arrive on an mbarrier of another CTA of the cluster (address from mapa_shared). The default
+// semantics (release at CTA scope): what the partner waits for here is tensor memory, ordered by
+// tcgen05.wait::st and tcgen05.fence::before_thread_sync ahead of the arrive, or the end of this
+// CTA's tensor-memory loads; a cluster-scope release costed a dequant warp ~2,400 cycles a stage.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // try_wait with cluster-scope acquire: for barriers that other CTAs of the cluster arrive on.
