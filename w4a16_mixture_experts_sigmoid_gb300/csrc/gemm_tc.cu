@@ -375,11 +375,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + sw * C::kWStage);
           const uint32_t sb = smem_u32(bring + sbi * C::kBStage);
+          const uint64_t bdesc0 = sw128_kmajor_desc(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const int sub = kk >> 2;
             const uint32_t koff = (kk & 3) * 32;
-            const uint64_t bdesc = sw128_kmajor_desc(sb + sub * (NT * 128) + koff);
+            // K step kk: the stage's descriptor plus a constant (the start-address field counts
+            // 16-byte units and cannot carry out: shared memory is below 2^18 bytes)
+            const uint64_t bdesc = bdesc0 + ((sub * (NT * 128) + koff) >> 4);
             const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
             if (ASRC == A_TMEM_DQ) {
               mma_ts(d_tmem, tmem + b * 128 + kk * 8, bdesc, idesc, acc);
