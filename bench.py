@@ -195,7 +195,7 @@ def profile_traffic(kernel_tag: str, workload: str):
 
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "common.cuh"):
+    for f in ("gemm_tc.cu", "gemm_pair.cu", "gemm_tc_parts.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "w4a16_mixture_experts_sigmoid_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
