@@ -60,6 +60,9 @@ WORKLOADS = {
     # the decode layer with its routed bank in pinned host memory: each step copies the touched experts
     # over the host link into a device bank, then runs the layer there
     "decode_t64_offload": dict(shape=synth.FULL, T=64, skew=None, offload=True),
+    # the decode layer from the token activations alone: router logits projected from x with a bf16 gate
+    # matrix [E, H] (N(0, 1/H): about N(0, 1) logits), then the layer
+    "decode_t64_router": dict(shape=synth.FULL, T=64, skew=None, router=True),
     "prefill_t4096_zipf_nvfp4": dict(shape=synth.FULL, T=4096, skew=1.1, fmt="nvfp4"),
 }
 
@@ -359,6 +362,7 @@ def run_ours(args):
     s = w["shape"]
     T = w["T"]
     fp4 = w.get("fmt") == "nvfp4"
+    router = bool(w.get("router"))
     arrays, x, logits = make_inputs(w, seed=0)
     layer = (MoeFp4Layer if fp4 else MoeW4A16Layer).from_arrays(s, arrays, device=dev)
     gemm_call = B.moe_fp4_grouped_gemm if fp4 else B.moe_w4a16_grouped_gemm
@@ -367,13 +371,24 @@ def run_ours(args):
     out = torch.empty((T, s.H), dtype=torch.int16, device=dev)
     flags = args.flags
     stream = torch.cuda.current_stream(dev)
+    if router:
+        gate = torch.from_numpy(synth.make_gate(s.E, s.H, seed=1).view(np.int16)).to(dev)
+        wsr = torch.zeros(B.moe_workspace_size(layer.dims, T, s.shared_I, B.MOE_FLAG_ROUTER_PROJECT),
+                          dtype=torch.uint8, device=dev)
+        rws = torch.zeros(B.moe_router_workspace_size(T, s.E, s.H), dtype=torch.uint8, device=dev)
+        B.moe_router_logits(xd, gate, T, s.E, s.H, ld, rws)      # the logits the split calls below route
 
     def step():
-        layer.forward(xd, ld, out=out, flags=flags)
+        if router:
+            B.moe_forward_project(layer.dims, layer.weights, gate, xd, T, out, wsr, flags)
+        else:
+            layer.forward(xd, ld, out=out, flags=flags)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    if router and B.moe_check_status(wsr) != 0:
+        raise RuntimeError("device status after warm-up (router projection)")
     st = layer.check_status()
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {B.moe_status_string(st)}")
@@ -429,7 +444,7 @@ def run_ours(args):
     # per-kernel pass: the same kernels through the split entry points, events between them (the
     # shared expert, when the layer has one, as one entry: its two GEMMs and their K-slice finishes)
     ksteps = max(10, min(args.steps, 100))
-    names = ["route", "permute_gather", "gemm_gate_up", "gemm_down"]
+    names = (["router_logits"] if router else []) + ["route", "permute_gather", "gemm_gate_up", "gemm_down"]
     ys = None
     if s.shared_I:
         names.append("shared_expert")
@@ -438,16 +453,21 @@ def run_ours(args):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(ksteps)]
     for i in range(ksteps):
         E_ = ev[i]
-        E_[0].record(stream)
+        j = 0
+        E_[j].record(stream)
+        if router:
+            B.moe_router_logits(xd, gate, T, s.E, s.H, ld, rws, flags)
+            j += 1
+            E_[j].record(stream)
         B.moe_route(ld, T, s.E, s.top_k, d_ids, d_w)
-        E_[1].record(stream)
+        E_[j + 1].record(stream)
         B.moe_permute(d_ids, T, s.E, s.top_k, d_off, d_srt, d_inv, xd, s.H, xperm, wsp, order)
-        E_[2].record(stream)
+        E_[j + 2].record(stream)
         gemm_call(B.MOE_GEMM_GATEUP_SILU, layer.dims, layer.weights, xperm, T, d_off, h, wsp, flags | order)
-        E_[3].record(stream)
+        E_[j + 3].record(stream)
         gemm_call(B.MOE_GEMM_DOWN, layer.dims, layer.weights, h, T, d_off, y, wsp, flags | order | B.MOE_FLAG_OUT_F32)
-        E_[4].record(stream)
-        j = 5
+        E_[j + 4].record(stream)
+        j += 5
         if ys is not None:
             B.moe_shared_expert(layer.dims, layer.weights, xd, T, ys, wsp, flags | B.MOE_FLAG_OUT_F32)
             E_[j].record(stream)
@@ -464,6 +484,11 @@ def run_ours(args):
     }
     flops = {"gemm_gate_up": 2.0 * R * s.H * 2 * s.I, "gemm_down": 2.0 * R * s.I * s.H}
     gemms = ["gemm_gate_up", "gemm_down"]
+    if router:
+        # bf16 gate [E][H] and x in, fp32 logits out
+        alg["router_logits"] = s.E * s.H * 2 + T * s.H * 2 + T * s.E * 4
+        flops["router_logits"] = 2.0 * T * s.E * s.H
+        gemms.append("router_logits")
     if s.shared_I:
         # bf16 weights [2Is][H] and [H][Is], x in, the result out (the intermediate is not counted)
         alg["shared_expert"] = 3 * s.H * s.shared_I * 2 + 2 * T * s.H * 2
@@ -479,6 +504,9 @@ def run_ours(args):
     if s.shared_I:
         step_bytes += 3 * s.H * s.shared_I * 2
     step_flops = 6.0 * T * s.top_k * s.H * s.I + (6.0 * T * s.H * s.shared_I)
+    if router:
+        step_bytes += s.E * s.H * 2
+        step_flops += 2.0 * T * s.E * s.H
     t_hbm = step_bytes / (hbm * 1e9)
     t_tc = step_flops / (bf16_sus * 1e12)
     step_roof = {"touched_experts": touched, "bytes": step_bytes, "flops": step_flops,
@@ -494,7 +522,11 @@ def run_ours(args):
     xe, le = torch.empty_like(xd), torch.empty_like(ld)
 
     def e2e_step():
-        if fp4:   # pinned host buffers through torch copies on the stream around moe_forward_fp4
+        if router:  # pinned host x only (the logits are projected on the device)
+            xe.copy_(xh, non_blocking=True)
+            B.moe_forward_project(layer.dims, layer.weights, gate, xe, T, out, wsr, flags)
+            oh.copy_(out, non_blocking=True)
+        elif fp4:   # pinned host buffers through torch copies on the stream around moe_forward_fp4
             xe.copy_(xh, non_blocking=True)
             le.copy_(lh, non_blocking=True)
             layer.forward(xe, le, out=out, flags=flags)
@@ -513,9 +545,11 @@ def run_ours(args):
         e2e_step()
         torch.cuda.current_stream(dev).synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / esteps, dev)
-    e2e = {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": x.nbytes + logits.nbytes,
+    e2e = {"value": whole_job_tokens_per_s(T, world, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": x.nbytes + (0 if router else logits.nbytes),
            "d2h_bytes_per_step": T * s.H * 2, "ms_per_step": e2e_s * 1e3,
-           "note": ("pinned host x/logits -> device (torch copies on the stream), moe_forward_fp4, result -> "
+           "note": ("pinned host x -> device, moe_forward_project, result -> pinned host" if router else
+                    "pinned host x/logits -> device (torch copies on the stream), moe_forward_fp4, result -> "
                     "pinned host" if fp4 else "moe_forward_host: pinned host x/logits -> device, layer, result -> "
                     "pinned host") + ", stream synchronised every step"}
 
