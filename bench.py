@@ -196,9 +196,13 @@ def profile_traffic(kernel_tag: str, workload: str):
     return float(m_b.group(1))
 
 
+# the sources of the grouped-GEMM kernels whose ncu summaries bench reads traffic from
+KERNEL_SOURCES = ("gemm_tc.cu", "gemm_pair.cu", "gemm_tc_parts.cuh", "common.cuh")
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemm_pair.cu", "gemm_tc_parts.cuh", "common.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "w4a16_mixture_experts_sigmoid_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()

@@ -81,7 +81,7 @@ def test_profile_traffic_only_for_the_captured_source(monkeypatch, tmp_path):
     real_root = bench.ROOT
     csrc = tmp_path / "w4a16_mixture_experts_sigmoid_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for f in ("gemm_tc.cu", "common.cuh"):
+    for f in bench.KERNEL_SOURCES:
         (csrc / f).write_bytes(open(f"{real_root}/w4a16_mixture_experts_sigmoid_gb300/csrc/{f}", "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profile_traffic("gemm_gate_up", "w1") == 4.8e9
