@@ -64,7 +64,9 @@ struct PairCfg {
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-template <int OP, int NT, int FMT>
+// YF32 (down only): fp32 rows to p.out_f32 instead of bf16 to p.out, chosen at compile time (a run-time
+// branch in the epilogue costs the down kernels ~25%)
+template <int OP, int NT, int FMT, bool YF32>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ TcParams p) {
   using C = PairCfg<NT>;
   constexpr int SW = C::kWStages;
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
               const int row = ti.row0 + cb + c;
               if (cb + c < ti.nvalid && row < p.R) {
                 const int64_t o = static_cast<int64_t>(row) * p.out_cols + n;
-                if (p.out_f32 != nullptr) p.out_f32[o] = __uint_as_float(v[c]);
+                if (YF32) p.out_f32[o] = __uint_as_float(v[c]);
                 else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
               }
             }
@@ -462,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 }
 
 // Clusters of two that can be resident at once, per device ordinal and kernel.
-template <int OP, int NT, int FMT>
+template <int OP, int NT, int FMT, bool YF32>
 int max_pairs(cudaStream_t s, int num_sms) {
   static std::atomic<int> cached[64];
   int dev = 0;
@@ -482,7 +484,7 @@ int max_pairs(cudaStream_t s, int num_sms) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<OP, NT, FMT>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<OP, NT, FMT, YF32>, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = num_sms / 2;
   }
@@ -490,8 +492,8 @@ int max_pairs(cudaStream_t s, int num_sms) {
   return n;
 }
 
-template <int OP, int NT, int FMT>
-cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaStream_t s) {
+template <int OP, int NT, int FMT, bool YF32>
+cudaError_t run_pair_y(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaStream_t s) {
   using C = PairCfg<NT>;
   static std::atomic<uint64_t> opted_in{0};
   int dev = 0;
@@ -499,12 +501,12 @@ cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaS
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || !(opted_in.load() & bit)) {
-    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<OP, NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<OP, NT, FMT, YF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  const int cap = max_pairs<OP, NT, FMT>(s, num_sms);
+  const int cap = max_pairs<OP, NT, FMT, YF32>(s, num_sms);
   const int pairs = static_cast<int>(pair_tiles < cap ? pair_tiles : cap);
   if (pairs <= 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
@@ -521,10 +523,17 @@ cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaS
   at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<OP, NT, FMT>, prm);
+  e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<OP, NT, FMT, YF32>, prm);
   count_launches(1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int OP, int NT, int FMT>
+cudaError_t run_pair(const TcParams& prm, int64_t pair_tiles, int num_sms, cudaStream_t s) {
+  if (OP == MOE_GEMM_DOWN && prm.out_f32 != nullptr)
+    return run_pair_y<OP, NT, FMT, OP == MOE_GEMM_DOWN>(prm, pair_tiles, num_sms, s);
+  return run_pair_y<OP, NT, FMT, false>(prm, pair_tiles, num_sms, s);
 }
 
 template <int OP, int FMT>

@@ -108,7 +108,10 @@ struct Cfg {
   static_assert(kWStage % 1024 == 0 && kBStage % 1024 == 0, "stages must keep 1024-byte alignment");
 };
 
-template <int OP, int ASRC, int NT, int FMT = WFMT_INT4>
+// YF32 (down only): the rows are written in fp32 to p.out_f32 instead of bf16 to p.out. A compile-time
+// choice: a run-time branch on the output type in the epilogue made the down kernel ~25% slower at
+// 32- and 128-token tiles, whichever type it wrote.
+template <int OP, int ASRC, int NT, int FMT = WFMT_INT4, bool YF32 = false>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<ASRC, NT>;
   constexpr int SW = C::kWStages;
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               const int row = ti.row0 + cb + c;
               if (cb + c < ti.nvalid && row < p.R) {
                 const int64_t o = static_cast<int64_t>(row) * p.out_cols + n;
-                if (p.out_f32 != nullptr) p.out_f32[o] = __uint_as_float(v[c]);
+                if (YF32) p.out_f32[o] = __uint_as_float(v[c]);
                 else p.out[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[c])));
               }
             }
@@ -584,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 // host side
 // ---------------------------------------------------------------------------
 
-template <int OP, int ASRC, int NT, int FMT = WFMT_INT4>
-cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
+template <int OP, int ASRC, int NT, int FMT, bool YF32>
+cudaError_t run_y(const TcParams& prm, int grid, cudaStream_t s) {
   using C = Cfg<ASRC, NT>;
   // the shared-memory opt-in is per device: remember it per device ordinal
   static std::atomic<uint64_t> opted_in{0};
@@ -594,14 +597,21 @@ cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || !(opted_in.load() & bit)) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel<OP, ASRC, NT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tc_gemm_kernel<OP, ASRC, NT, FMT, YF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  (void)launch_pdl(tc_gemm_kernel<OP, ASRC, NT, FMT>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, prm);
+  (void)launch_pdl(tc_gemm_kernel<OP, ASRC, NT, FMT, YF32>, dim3(grid), dim3(kThreads), C::kSmemBytes, s, prm);
   count_launches(1);
   return cudaGetLastError();
+}
+
+// the down kernels come in both output types; gate/up writes bf16 h only
+template <int OP, int ASRC, int NT, int FMT = WFMT_INT4>
+cudaError_t run(const TcParams& prm, int grid, cudaStream_t s) {
+  if (OP == MOE_GEMM_DOWN && prm.out_f32 != nullptr) return run_y<OP, ASRC, NT, FMT, OP == MOE_GEMM_DOWN>(prm, grid, s);
+  return run_y<OP, ASRC, NT, FMT, false>(prm, grid, s);
 }
 
 // After a launch with K slices: out[r][c] = bf16 of the finished sums, the slices added in order
