@@ -278,14 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     __syncwarp();
   } else if (warp == 1 || (C::kMmaGroups == 2 && warp == kSecondMmaWarp)) {
     // ------------------------------------------------------------ MMA issuers (CTA 0 only)
-    if (lane == 0 && rank == 0) {
+    // with 128-token tiles the whole warp runs the loop and one elected lane issues (iss_wait)
+    constexpr bool W = NT >= 128;
+    if (rank == 0 && (W || lane == 0)) {
       constexpr uint32_t idesc = idesc_bf16_f32(2 * BM, NT);
       const int mg = (warp == 1) ? 0 : 1;
       int g = 0, it = 0;
       bool ok = true;
       for (int i = pair; i < total && ok; i += n_pairs, ++it) {
         const int ab = it & 1;
-        if (!mbar_wait_cluster(&accempty[ab], ((it >> 1) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
+        if (!iss_wait_cluster<W>(&accempty[ab], ((it >> 1) & 1) ^ 1, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol + (mg * 2 + ab) * NT;
         bool first = true;
@@ -293,13 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           if (C::kMmaGroups == 2 && (g & 1) != mg) continue;
           const int sbi = g % SB;
           const int b = g % NB;
-          if (!mbar_wait_cluster(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p.timeout_ns, abort_flag,
-                                 p.status)) {
+          if (!iss_wait_cluster<W>(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p, abort_flag)) {
             ok = false;
             break;
           }
-          if (!mbar_wait_cluster(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p.timeout_ns, abort_flag,
-                                 p.status)) {
+          if (!iss_wait_cluster<W>(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p, abort_flag)) {
             ok = false;
             break;
           }
@@ -311,17 +311,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
             // counts 16-byte units and cannot carry out: shared memory is below 2^18 bytes)
             const uint32_t off = (kk >> 2) * (C::kHalf * 128) + (kk & 3) * 32;
             const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
-            mma_ts_pair(d_tmem, tmem + b * 128 + kk * 8, bdesc0 + (off >> 4), idesc, acc);
+            iss_mma_ts_pair<W>(d_tmem, tmem + b * 128 + kk * 8, bdesc0 + (off >> 4), idesc, acc);
           }
           first = false;
-          if (!C::kBViaA) mma_commit_pair(&bempty[sbi], 3);
-          mma_commit_pair(&aempty[((g + NB) & 1) * NB + b], 3);
+          if (!C::kBViaA) iss_commit_pair<W>(&bempty[sbi], 3);
+          iss_commit_pair<W>(&aempty[((g + NB) & 1) * NB + b], 3);
         }
         if (!ok) break;
-        mma_commit_pair(&accfull[ab], 3);
+        iss_commit_pair<W>(&accfull[ab], 3);
       }
-      mma_commit_pair(drain, 3);
-      mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status);
+      iss_commit_pair<W>(drain, 3);
+      iss_wait<W>(drain, 0, p, nullptr);
     }
     __syncwarp();
   } else if (warp >= kFirstDqWarp && warp < kFirstEpiWarp) {

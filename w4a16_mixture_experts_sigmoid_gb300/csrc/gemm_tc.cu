@@ -26,13 +26,15 @@
 //               words + bf16 scales (or dense bf16 weights) into the weight ring.
 //   warp 14     token-row producer: TMA of the token rows into their ring; a
 //               warp of its own so that the weight stream never waits on it.
-//   warps 1, 15 MMA issuers (lane 0 each; warp 1 also owns the tensor-memory
-//               allocation). A thread can issue one M=128 MMA about every 45
-//               cycles whatever N is, while the tensor core accepts MMAs from
-//               several threads at once; so each of the two dequant groups
-//               has its own issuer and its own fp32 accumulators, and the
-//               epilogue adds the two. (With 128 tokens per tile one issuer
-//               keeps up with the math, and tensor memory holds one set.)
+//   warps 1, 15 MMA issuers (lane 0 each, or with 128-token tiles the whole
+//               warp with one elected lane issuing; warp 1 also owns the
+//               tensor-memory allocation). A thread can issue one M=128 MMA
+//               about every 50 cycles whatever N <= 64 is, while the tensor
+//               core accepts MMAs from several threads at once; so each of
+//               the two dequant groups has its own issuer and its own fp32
+//               accumulators, and the epilogue adds the two. (With 128 tokens
+//               per tile one issuer keeps up with the math, and tensor memory
+//               holds one set.)
 //   warps 2-9   dequantise, in two groups of four that take alternate stages:
 //               each thread owns one weight row (= one TMEM lane) of its
 //               group's stage and turns its 256 nibbles into bf16(q*s) in the
@@ -345,14 +347,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     __syncwarp();
   } else if (warp == 1 || (C::kMmaGroups == 2 && warp == kSecondMmaWarp)) {
     // ------------------------------------------------------------ MMA issuers
-    if (lane == 0) {
+    // With 128-token tiles the whole warp runs the loop and one elected lane issues (iss_wait)
+    constexpr bool W = NT >= 128;
+    if (W || lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, NT);
       const int mg = (warp == 1) ? 0 : 1;  // with two issuers, issuer mg takes the stages g with g % 2 == mg
       int g = 0, it = 0;
       bool ok = true;
       for (int i = blockIdx.x; i < total && ok; i += gridDim.x, ++it) {
         const int ab = it & 1;
-        if (!mbar_wait(&accempty[ab], ((it >> 1) & 1) ^ 1, p.timeout_ns, abort_flag, p.status)) break;
+        if (!iss_wait<W>(&accempty[ab], ((it >> 1) & 1) ^ 1, p, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + C::kAccCol + (mg * 2 + ab) * NT;
         bool first = true;
@@ -360,17 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (C::kMmaGroups == 2 && (g & 1) != mg) continue;
           const int sw = g % SW, sbi = g % SB;
           const int b = g % NB;
-          if (!mbar_wait(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+          if (!iss_wait<W>(&bfull[(g & 1) * SB + sbi], (g / C::kBPeriod) & 1, p, abort_flag)) {
             ok = false;
             break;
           }
           if (C::kDq) {
-            if (!mbar_wait(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+            if (!iss_wait<W>(&afull[(g & 1) * NB + b], (g / C::kAPeriod) & 1, p, abort_flag)) {
               ok = false;
               break;
             }
           } else {
-            if (!mbar_wait(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p.timeout_ns, abort_flag, p.status)) {
+            if (!iss_wait<W>(&wfull[(g & 1) * SW + sw], (g / C::kWPeriod) & 1, p, abort_flag)) {
               ok = false;
               break;
             }
@@ -388,26 +392,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const uint64_t bdesc = bdesc0 + ((sub * (NT * 128) + koff) >> 4);
             const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
             if (ASRC == A_TMEM_DQ) {
-              mma_ts(d_tmem, tmem + b * 128 + kk * 8, bdesc, idesc, acc);
+              iss_mma_ts<W>(d_tmem, tmem + b * 128 + kk * 8, bdesc, idesc, acc);
             } else if (ASRC == A_SMEM_DQ) {
               const uint64_t adesc = sw128_kmajor_desc(smem_u32(abuf + b * C::kABuf) + sub * (BM * 128) + koff);
-              mma_ss(d_tmem, adesc, bdesc, idesc, acc);
+              iss_mma_ss<W>(d_tmem, adesc, bdesc, idesc, acc);
             } else {
               const uint64_t adesc = sw128_kmajor_desc(sa + sub * (BM * 128) + koff);
-              mma_ss(d_tmem, adesc, bdesc, idesc, acc);
+              iss_mma_ss<W>(d_tmem, adesc, bdesc, idesc, acc);
             }
           }
           first = false;
-          if (!C::kBViaA) mma_commit(&bempty[sbi]);
-          if (C::kDq) mma_commit(&aempty[((g + NB) & 1) * NB + b]);   // to the group of the next user
-          else mma_commit(&wempty[sw]);
+          if (!C::kBViaA) iss_commit<W>(&bempty[sbi]);
+          if (C::kDq) iss_commit<W>(&aempty[((g + NB) & 1) * NB + b]);   // to the group of the next user
+          else iss_commit<W>(&wempty[sw]);
         }
         if (!ok) break;
-        mma_commit(&accfull[ab]);   // an issuer with no stage in this tile arrives at once
+        iss_commit<W>(&accfull[ab]);   // an issuer with no stage in this tile arrives at once
       }
       // let every MMA issued by this thread finish before tensor memory is freed
-      mma_commit(drain);
-      mbar_wait(drain, 0, p.timeout_ns, nullptr, p.status);
+      iss_commit<W>(drain);
+      iss_wait<W>(drain, 0, p, nullptr);
     }
     __syncwarp();
   } else if (warp >= kFirstDqWarp && warp < kFirstEpiWarp) {

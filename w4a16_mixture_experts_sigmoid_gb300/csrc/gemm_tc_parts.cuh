@@ -93,6 +93,61 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
+// MMA issue in one of two forms, chosen per kernel at compile time. WARP: the whole issuer warp
+// runs the loop in lockstep (warp_wait) and one elected lane issues each MMA and commit (the
+// *_elect forms); with 128-token tiles this made the gate/up GEMM 2% and the pair down GEMM 7%
+// faster at prefill. Otherwise lane 0 alone runs the loop, which measured 4% faster for the
+// 16- to 64-token tiles of decode.
+template <bool WARP>
+__device__ __forceinline__ bool iss_wait(uint64_t* bar, uint32_t parity, const TcParams& p, volatile int* abort_flag) {
+  if (WARP) return warp_wait(bar, parity, p, abort_flag);
+  return mbar_wait(bar, parity, p.timeout_ns, abort_flag, p.status);
+}
+
+template <bool WARP>
+__device__ __forceinline__ void iss_mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (WARP) mma_ts_elect(d, a, b, idesc, acc);
+  else mma_ts(d, a, b, idesc, acc);
+}
+
+template <bool WARP>
+__device__ __forceinline__ void iss_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (WARP) mma_ss_elect(d, a, b, idesc, acc);
+  else mma_ss(d, a, b, idesc, acc);
+}
+
+template <bool WARP>
+__device__ __forceinline__ void iss_commit(uint64_t* bar) {
+  if (WARP) mma_commit_elect(bar);
+  else mma_commit(bar);
+}
+
+// The same with cluster-scope acquire (barriers that the peer CTA of a pair arrives on).
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, const TcParams& p,
+                                                  volatile int* abort_flag) {
+  const bool ok = mbar_wait_cluster(bar, parity, p.timeout_ns, abort_flag, p.status);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+template <bool WARP>
+__device__ __forceinline__ bool iss_wait_cluster(uint64_t* bar, uint32_t parity, const TcParams& p,
+                                                 volatile int* abort_flag) {
+  if (WARP) return warp_wait_cluster(bar, parity, p, abort_flag);
+  return mbar_wait_cluster(bar, parity, p.timeout_ns, abort_flag, p.status);
+}
+
+template <bool WARP>
+__device__ __forceinline__ void iss_mma_ts_pair(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (WARP) mma_ts_pair_elect(d, a, b, idesc, acc);
+  else mma_ts_pair(d, a, b, idesc, acc);
+}
+
+template <bool WARP>
+__device__ __forceinline__ void iss_commit_pair(uint64_t* bar, uint16_t mask) {
+  if (WARP) mma_commit_pair_elect(bar, mask);
+  else mma_commit_pair(bar, mask);
+}
+
 // One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
 // 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
 // 8i+m (low half) and 8i+m+4 (high half) of the chunk. Per pair of weights:
