@@ -235,11 +235,12 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, 
     p.a = scratch;
     p.a_mma_order = true;
   }
-  // CTA pairs: one pair MMA covers 256 weight rows over two SMs (A in tensor memory only). On by
-  // request, and by default for the down projection of prefill-shaped batches (128-token tiles),
-  // where it measured faster than one CTA (prefill_t4096_zipf: 1.64 against 1.76 ms); at decode
-  // sizes and for gate/up one CTA per tile is as fast or faster.
-  const bool pair_auto = auto_nt && nt == 128 && op == MOE_GEMM_DOWN && !(flags & MOE_FLAG_A_SMEM);
+  // CTA pairs: one pair MMA covers 256 weight rows over two SMs (A in tensor memory only), and
+  // each CTA loads half of the token rows, so a 128-token tile's B ring has five stages instead
+  // of two. On by request, and by default for prefill-shaped batches (128-token tiles), where
+  // it measured faster than one CTA (prefill_t4096_zipf: down 1.37 against 1.76 ms, gate/up
+  // 2.55 against 2.60 ms); at decode sizes one CTA per tile is as fast or faster.
+  const bool pair_auto = auto_nt && nt == 128 && !(flags & MOE_FLAG_A_SMEM);
   const bool pair = ((flags & MOE_FLAG_GEMM_PAIR) != 0 || pair_auto) && asrc == A_TMEM_DQ;
   auto launch = [&](const GemmProblem& q, int tiles_nt) {
     return pair ? launch_gemm_pair(q, tiles_nt, sms, s) : launch_gemm_tc(q, asrc, tiles_nt, sms, s);
