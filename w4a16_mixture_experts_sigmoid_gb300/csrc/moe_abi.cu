@@ -237,12 +237,14 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, 
   }
   // CTA pairs: one pair MMA covers 256 weight rows over two SMs (A in tensor memory only), and
   // each CTA loads half of the token rows, so a 128-token tile's B ring has five stages instead
-  // of two. On by request, and by default for prefill-shaped batches (128-token tiles), where
-  // it measured faster than one CTA (prefill_t4096_zipf: down 1.37 against 1.76 ms, gate/up
-  // 2.55 against 2.60 ms); at decode sizes one CTA per tile is as fast or faster.
-  const bool pair_auto = auto_nt && nt == 128 && !(flags & MOE_FLAG_A_SMEM);
-  const bool pair = ((flags & MOE_FLAG_GEMM_PAIR) != 0 || pair_auto) && asrc == A_TMEM_DQ;
-  auto launch = [&](const GemmProblem& q, int tiles_nt) {
+  // of two. On by request, and by default for the launches of prefill-shaped batches where it
+  // measured faster than one CTA per tile (prefill_t4096_zipf): both down launches (1.64 against
+  // 1.76 ms together) and the gate/up launch with 128-token tiles (1.50 against 1.58 ms, cold
+  // serialised launches); the gate/up launch with 32-token tiles was 5% slower on pairs (0.96
+  // against 0.92 ms), and at decode sizes one CTA per tile is as fast or faster.
+  const bool pair_req = (flags & MOE_FLAG_GEMM_PAIR) != 0;
+  auto launch = [&](const GemmProblem& q, int tiles_nt, bool pair_default) {
+    const bool pair = (pair_req || (pair_default && !(flags & MOE_FLAG_A_SMEM))) && asrc == A_TMEM_DQ;
     return pair ? launch_gemm_pair(q, tiles_nt, sms, s) : launch_gemm_tc(q, asrc, tiles_nt, sms, s);
   };
   cudaError_t e;
@@ -253,14 +255,14 @@ moe_status_t run_grouped_gemm(int32_t op, const moe_dims_t& d, const LayerW& w, 
     // its experts, found from the offsets on the device.
     GemmProblem small = p;
     small.max_rows = 32;
-    e = launch(small, 32);
+    e = launch(small, 32, op == MOE_GEMM_DOWN);
     if (e == cudaSuccess) {
       GemmProblem big = p;
       big.min_rows = 33;
-      e = launch(big, 128);
+      e = launch(big, 128, true);
     }
   } else {
-    e = launch(p, nt);
+    e = launch(p, nt, false);
   }
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED_SHAPE;
   return cuda_status(e);
