@@ -566,7 +566,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(args.workload, w), "T": T, "E": s.E, "top_k": s.top_k, "H": s.H,
                    "I": s.I, "shared_I": s.shared_I, "parallelism": f"replicas x{world}",
-                   "l2": f"no flush: each step streams {touched} experts' int4 weights "
+                   "l2": f"no flush: each step streams {touched} experts' {'E2M1' if fp4 else 'int4'} weights "
                          f"({touched * (gu_b + dn_b) / 1e9:.2f} GB) through a 129 MB L2",
                    "flags": flags},
         "roofline": roofline, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
