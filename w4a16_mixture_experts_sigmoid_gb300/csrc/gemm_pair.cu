@@ -26,6 +26,7 @@
 
 #include <atomic>
 #include <cstring>
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -345,38 +346,45 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         uint4 wv[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
-        constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
-        uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
+        // the conversion's form, once per stage for the whole warp (as in the single-CTA kernel)
+        const bool fast = (FMT == WFMT_INT4) && __all_sync(0xFFFFFFFFu, int4_row_fast(sw4));
+        auto convert = [&](auto fast_tag) -> bool {
+          constexpr bool kFast = decltype(fast_tag)::value;
+          constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
+          uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
 #pragma unroll
-        for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT>(wv[c], sw4, c, pre[c]);
-        if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+          for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT, kFast>(wv[c], sw4, c, pre[c]);
+          if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) return false;
+          tc_fence_after();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (half == 1) {
+          for (int half = 0; half < 2; ++half) {
+            if (half == 1) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[sw]);
+              for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&wempty[sw]);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int c = half * 4 + cc;
+              uint32_t dqc[16];
+              if (c >= kPreChunks) dequant_chunk<FMT, kFast>(wv[cc], sw4, c, dqc);
+              const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
+              tmem_st8(lane_base + b * 128 + c * 16, dq);
+              tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
+            }
           }
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int c = half * 4 + cc;
-            uint32_t dqc[16];
-            if (c >= kPreChunks) dequant_chunk<FMT>(wv[cc], sw4, c, dqc);
-            const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
-            tmem_st8(lane_base + b * 128 + c * 16, dq);
-            tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            uint64_t* af = &afull[grp * NB + b];
+            if (rank == 0) mbar_arrive(af);
+            else mbar_arrive_remote(mapa_shared(smem_u32(af), 0));
           }
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          uint64_t* af = &afull[grp * NB + b];
-          if (rank == 0) mbar_arrive(af);
-          else mbar_arrive_remote(mapa_shared(smem_u32(af), 0));
-        }
+          return true;
+        };
+        if (!(fast ? convert(std::true_type{}) : convert(std::false_type{}))) { ok = false; break; }
       }
     }
   } else if (warp >= kFirstEpiWarp && warp < kFirstEpiWarp + 4) {

@@ -60,6 +60,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 namespace moe {
 namespace {
@@ -446,48 +447,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           for (int c = 0; c < 4; ++c)
             wv[c] = (OP == MOE_GEMM_GATEUP_SILU) ? ld_shared_v4((smem_u32(smem + sw * C::kWStage) + row_x) ^ (c << 4))
                                                  : *reinterpret_cast<const uint4*>(arow + ((c ^ (r_sm & 7)) << 4));
-          // The first half row's conversion needs no A buffer, so for gate/up it runs before the
-          // wait for one (gate/up 3% faster at decode; the same for down made it 2% slower).
-          constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
-          uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
+          // The conversion's form (dequant_group) is chosen once per stage for the whole warp: the
+          // exact fma form when every scale of the warp's rows allows it, else the general one.
+          const bool fast = (FMT == WFMT_INT4) && __all_sync(0xFFFFFFFFu, int4_row_fast(sw4));
+          auto convert = [&](auto fast_tag) -> bool {
+            constexpr bool kFast = decltype(fast_tag)::value;
+            // The first half row's conversion needs no A buffer, so for gate/up it runs before the
+            // wait for one (gate/up 3% faster at decode; the same for down made it 2% slower).
+            constexpr int kPreChunks = (OP == MOE_GEMM_GATEUP_SILU) ? 4 : 0;
+            uint32_t pre[kPreChunks > 0 ? kPreChunks : 1][16];
 #pragma unroll
-          for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT>(wv[c], sw4, c, pre[c]);
-          if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) { ok = false; break; }
-          tc_fence_after();
+            for (int c = 0; c < kPreChunks; ++c) dequant_chunk<FMT, kFast>(wv[c], sw4, c, pre[c]);
+            if (a_need > 0 && !warp_wait(&aempty[grp * NB + b], (a_need - 1) & 1, p, abort_flag)) return false;
+            tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (half == 1) {
+            for (int half = 0; half < 2; ++half) {
+              if (half == 1) {
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
-                wv[c] = (OP == MOE_GEMM_GATEUP_SILU)
-                            ? ld_shared_v4((smem_u32(smem + sw * C::kWStage) + row_x) ^ ((c + 4) << 4))
-                            : *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&wempty[sw]);
-            }
+                for (int c = 0; c < 4; ++c)
+                  wv[c] = (OP == MOE_GEMM_GATEUP_SILU)
+                              ? ld_shared_v4((smem_u32(smem + sw * C::kWStage) + row_x) ^ ((c + 4) << 4))
+                              : *reinterpret_cast<const uint4*>(arow + (((c + 4) ^ (r_sm & 7)) << 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wempty[sw]);
+              }
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const int c = half * 4 + cc;
-              uint32_t dqc[16];
-              if (c >= kPreChunks) dequant_chunk<FMT>(wv[cc], sw4, c, dqc);
-              const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
-              if (ASRC == A_TMEM_DQ) {
-                tmem_st8(lane_base + b * 128 + c * 16, dq);
-                tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
-              } else {
-                uint8_t* ab = abuf + b * C::kABuf + (c >> 1) * (BM * 128) + l * 128;
+              for (int cc = 0; cc < 4; ++cc) {
+                const int c = half * 4 + cc;
+                uint32_t dqc[16];
+                if (c >= kPreChunks) dequant_chunk<FMT, kFast>(wv[cc], sw4, c, dqc);
+                const uint32_t* dq = (c < kPreChunks) ? pre[c < kPreChunks ? c : 0] : dqc;
+                if (ASRC == A_TMEM_DQ) {
+                  tmem_st8(lane_base + b * 128 + c * 16, dq);
+                  tmem_st8(lane_base + b * 128 + c * 16 + 8, dq + 8);
+                } else {
+                  uint8_t* ab = abuf + b * C::kABuf + (c >> 1) * (BM * 128) + l * 128;
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-                  *reinterpret_cast<uint4*>(ab + ((((c & 1) * 4 + m) ^ (l & 7)) << 4)) =
-                      make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+                  for (int m = 0; m < 4; ++m)
+                    *reinterpret_cast<uint4*>(ab + ((((c & 1) * 4 + m) ^ (l & 7)) << 4)) =
+                        make_uint4(dq[4 * m], dq[4 * m + 1], dq[4 * m + 2], dq[4 * m + 3]);
+                }
               }
             }
-          }
-          if (ASRC == A_TMEM_DQ) tmem_wait_st();
-          else fence_proxy_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[grp * NB + b]);
+            if (ASRC == A_TMEM_DQ) tmem_wait_st();
+            else fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&afull[grp * NB + b]);
+            return true;
+          };
+          if (!(fast ? convert(std::true_type{}) : convert(std::false_type{}))) { ok = false; break; }
         }
       }
     }

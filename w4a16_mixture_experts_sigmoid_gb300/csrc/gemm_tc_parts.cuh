@@ -150,24 +150,63 @@ __device__ __forceinline__ void iss_commit_pair(uint64_t* bar, uint16_t mask) {
 
 // One 16-byte chunk = four int32 words = 32 inputs of one scale group ->
 // 16 bf16x2 registers in MMA K order: register 4i+m holds bf16(q*s) of inputs
-// 8i+m (low half) and 8i+m+4 (high half) of the chunk. Per pair of weights:
-// one lop3 makes the bf16 pattern 0x43<nibble> = 128 + nibble exactly, one
-// packed subtract of 136 gives q = nibble - 8 exactly, one packed multiply
-// rounds q*s once to nearest even. Written as PTX: the same two packed bf16
-// operations through the cuda_bf16 intrinsics take more issue slots.
-// s2: the group's bf16 scale in both halves.
+// 8i+m (low half) and 8i+m+4 (high half) of the chunk, q = nibble - 8. Two
+// exact forms; both round the exact product q*s once to nearest even, so they
+// agree bit for bit (up to the sign of a zero product):
+// * FAST, for 2^-126 <= |s| < 2^-5 (exponent field 1..121, which holds for
+//   every practical int4 group scale): a nibble n masked into a zero exponent
+//   field reads as the bf16 subnormal n * 2^-133, and one packed fma with
+//   S = s * 2^133 (133 added to s's exponent field, still a normal bf16) and
+//   C = -8 s (exact) gives n*s - 8s = q*s, computed exactly and rounded once:
+//   an AND (plus the shift) and an fma a pair.
+// * otherwise (any scale): one lop3 makes the bf16 pattern 0x43<nibble> =
+//   128 + n exactly, one packed subtract of 136 gives q exactly, one packed
+//   multiply rounds q*s once: a lop3, a subtract and a multiply a pair.
+// The form is chosen once per stage for a whole warp (int4_stage_fast): a
+// branch per chunk cost the kernels ~18% in instruction scheduling.
+// Written as PTX: the packed bf16 operations through the cuda_bf16 intrinsics
+// take more issue slots. s2: the group's bf16 scale in both halves.
+template <bool FAST>
 __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t s2, uint32_t* out16) {
   const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+  if (FAST) {
+    const uint32_t S2 = s2 + 0x42804280u;   // exponent field + 133 in both halves (no carry: <= 254)
+    uint32_t C2;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(C2) : "r"(s2), "r"(0xC100C100u));   // 0xC100 = bf16 -8
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      uint32_t pr, q;
-      asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(pr) : "r"(w4[i] >> (4 * m)), "r"(0x000F000Fu), "r"(0x43004300u));
-      asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(pr), "r"(0x43084308u));   // 0x4308 = bf16 136
-      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(q), "r"(s2));
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t t = (w4[i] >> (4 * m)) & 0x000F000Fu;   // n * 2^-133 in each half
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out16[4 * i + m]) : "r"(t), "r"(S2), "r"(C2));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t pr, q;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(pr) : "r"(w4[i] >> (4 * m)), "r"(0x000F000Fu), "r"(0x43004300u));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(q) : "r"(pr), "r"(0x43084308u));   // 0x4308 = bf16 136
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(q), "r"(s2));
+      }
     }
   }
+}
+
+// True when every one of a stage row's eight bf16 scales (sw4: four words of two) has its
+// exponent field in 1..121, the FAST form's range. Per half h: m = h & 0x7F80 is the exponent
+// field times 128; m + 0x4300 reaches bit 15 exactly when the field is >= 122, and m + 0x7F80
+// exactly when it is >= 1 (neither sum carries into the next half).
+__device__ __forceinline__ bool int4_row_fast(const uint32_t (&sw4)[4]) {
+  uint32_t bad = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t m = sw4[j] & 0x7F807F80u;
+    bad |= (m + 0x43004300u) | ~(m + 0x7F807F80u);
+  }
+  return (bad & 0x80008000u) == 0;
 }
 
 // The 4-bit float format: one 16-byte chunk of E2M1 codes = four words = 32 inputs, two blocks of
@@ -205,7 +244,7 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t b) {
 
 // Dequantise chunk c (0..7) of a stage row in the weight format FMT; sw4: the row's 16 scale bytes of
 // the stage (int4: eight bf16 scales, one per chunk; fp4: sixteen E4M3 scales, two per chunk).
-template <int FMT>
+template <int FMT, bool FAST = false>
 __device__ __forceinline__ void dequant_chunk(const uint4& wv, const uint32_t (&sw4)[4], int c, uint32_t* out16) {
   if (FMT == WFMT_FP4) {
     const uint32_t pair = (sw4[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu;   // scale bytes 2c, 2c + 1
@@ -213,7 +252,7 @@ __device__ __forceinline__ void dequant_chunk(const uint4& wv, const uint32_t (&
   } else {
     // chunk c's scale is half c % 2 of word c / 2: one byte permute copies it into both halves
     // (4% faster down GEMMs and 5% faster gate/up at 32-token tiles than a shift or mask and a multiply)
-    dequant_group(wv, __byte_perm(sw4[c >> 1], 0, (c & 1) ? 0x3232 : 0x1010), out16);
+    dequant_group<FAST>(wv, __byte_perm(sw4[c >> 1], 0, (c & 1) ? 0x3232 : 0x1010), out16);
   }
 }
 
