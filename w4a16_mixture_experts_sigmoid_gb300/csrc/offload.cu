@@ -31,13 +31,21 @@ struct StageArgs {
 
 // grid.x = E * chunks per expert (all four tensors). A block whose expert has no rows returns at
 // once; the others copy one slice of one tensor of their expert with 16-byte loads and stores.
+// The successor (the gate/up GEMM, one CTA per SM holding the whole register file) may launch
+// only as the copy's blocks finish: released at a block's start, its CTAs took SMs from the
+// copy's remaining blocks while they waited for it, and a step took up to 2.7 times as long.
 __global__ void __launch_bounds__(kStageThreads) stage_kernel(const __grid_constant__ StageArgs a) {
   griddep_wait();
-  griddep_launch();
   const int64_t per = a.chunk_base[4];
   const int e = static_cast<int>(blockIdx.x / per);
-  if (e >= a.E) return;
-  if (__ldg(a.offsets + e + 1) - __ldg(a.offsets + e) <= 0) return;
+  if (e >= a.E) {
+    griddep_launch();
+    return;
+  }
+  if (__ldg(a.offsets + e + 1) - __ldg(a.offsets + e) <= 0) {
+    griddep_launch();
+    return;
+  }
   int64_t c = blockIdx.x - static_cast<int64_t>(e) * per;
   int ti = 0;
   while (ti < 3 && c >= a.chunk_base[ti + 1]) ++ti;
@@ -59,6 +67,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_kernel(const __grid_const
     dst[i + 3 * kStageThreads] = v3;
   }
   for (; i < n; i += kStageThreads) dst[i] = src[i];
+  griddep_launch();
 }
 
 }  // namespace
