@@ -31,9 +31,9 @@ struct StageArgs {
 
 // grid.x = E * chunks per expert (all four tensors). A block whose expert has no rows returns at
 // once; the others copy one slice of one tensor of their expert with 16-byte loads and stores.
-// The successor (the gate/up GEMM, one CTA per SM holding the whole register file) may launch
-// only as the copy's blocks finish: released at a block's start, its CTAs took SMs from the
-// copy's remaining blocks while they waited for it, and a step took up to 2.7 times as long.
+// The successor (the gate/up GEMM, one CTA per SM holding the whole register file) is released
+// only as the copy's blocks finish, so that its CTAs, which wait for the whole copy anyway, do not
+// hold SMs that the copy's remaining blocks could use.
 __global__ void __launch_bounds__(kStageThreads) stage_kernel(const __grid_constant__ StageArgs a) {
   griddep_wait();
   const int64_t per = a.chunk_base[4];
