@@ -122,3 +122,36 @@ def test_fp4_full_size_decode_T64(cuda_lib):
     assert layer.check_status() == 0
     ref = oracle.moe_layer(x, logits, arrays, 8, workers=os.cpu_count() or 1)["out"]
     assert_close_rms(bf16_dev_to_f32(out), ref, what="fp4 decode T=64, all tokens")
+
+
+@pytest.mark.parametrize("impl", ["auto", "16", "128", "pair"])
+def test_fp4_dequantised_weights_bit_for_bit(cuda_lib, impl):
+    """One-hot down GEMMs (fp32 output) read single weights back: row j of expert e, one-hot at input
+    i, gives e2m1 * e4m3 * g, the exact product of the code and the block scale times the matrix
+    scale rounded once in fp32, as the oracle computes it. The scale bytes span every finite E4M3
+    code, subnormal to 448."""
+    import torch
+    from w4a16_mixture_experts_sigmoid_gb300 import binding as B
+    E, H, I = 2, 128, 512
+    layer = synth.make_layer_fp4(synth.LayerShape(E=E, top_k=1, H=H, I=I), seed=5)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)   # every finite code
+    layer["s2"] = codes[np.random.default_rng(6).integers(0, codes.size, size=layer["s2"].shape)]
+    T = E * I
+    offsets = np.arange(E + 1, dtype=np.int32) * I
+    rows = np.zeros((T, I), dtype=np.uint16)
+    rows[np.arange(T), np.arange(T) % I] = 0x3F80   # bf16 1.0
+    want = np.stack([oracle.dequant_fp4(layer["w2"][e], layer["s2"][e], layer["g2"][e]) for e in range(E)])
+    flags = {"auto": 0, "pair": B.MOE_FLAG_GEMM_PAIR | B.MOE_FLAG_TOKENS_PER_TILE(128)}.get(impl, 0)
+    if impl.isdigit():
+        flags = B.MOE_FLAG_TOKENS_PER_TILE(int(impl))
+    d = B.dims(E, 1, H, I, group=16)
+    w, _ = fp4_weights(B, layer)
+    ws = torch.zeros(B.moe_workspace_size(d, T), dtype=torch.uint8, device="cuda")
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.moe_fp4_grouped_gemm(B.MOE_GEMM_DOWN, d, w, dev(rows), T, dev(offsets), y, ws, flags | B.MOE_FLAG_OUT_F32)
+    assert B.moe_check_status(ws) == B.MOE_OK
+    got = host(y).reshape(E, I, H).transpose(0, 2, 1)
+    gb, wb = got.view(np.uint32), np.ascontiguousarray(want).view(np.uint32)
+    zero = (wb & 0x7FFFFFFF) == 0
+    assert np.array_equal(gb[~zero], wb[~zero]), f"{np.count_nonzero(gb[~zero] != wb[~zero])} weights differ"
+    assert np.all((gb[zero] & 0x7FFFFFFF) == 0)

@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             v[c] = use0 ? __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v1[c])) : v1[c];
         }
         if (FMT == WFMT_FP4) {
-          const float gs = __ldg(p.gscale + ti.e);   // the expert's fp32 matrix scale
+          const float gs = fp4_sum_scale(__ldg(p.gscale + ti.e));   // the expert's fp32 matrix scale, x 2^8
 #pragma unroll
           for (int c = 0; c < 16; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * gs);
         }

@@ -213,34 +213,44 @@ __device__ __forceinline__ bool int4_row_fast(const uint32_t (&sw4)[4]) {
 // 16 with their own scale, -> 16 bf16x2 registers in MMA K order (register 4i+m: inputs 8i+m and
 // 8i+m+4, as dequant_group). A code's magnitude bits (two exponent bits, one mantissa bit) moved to
 // bf16 bits 6..8 and its sign to bit 15 read as the code's value times 2^-126 (the codes +-0.5 as
-// bf16 subnormals); one packed multiply by 2^126 makes the value and one by the block's scale the
-// weight. Both products are exact: E2M1 values have two significant bits and E4M3 scales four.
-__device__ __forceinline__ void dequant_group_fp4(const uint4& wv, uint32_t s2_blk0, uint32_t s2_blk1,
+// bf16 subnormals); one packed multiply by the block's scale times 2^118 (fp4_block_scale) gives
+// the weight times 2^-8, exactly: E2M1 values have two significant bits and E4M3 scales four, and
+// every such product times 2^-8 is a normal bf16 (2^-18 .. 10.5). The epilogue multiplies the fp32
+// sums by the matrix scale times 2^8, which gives the same fp32 products as unscaled weights would.
+// Per pair: a shift or two, a select (lop3) of the magnitude and sign bits, an AND, a multiply.
+__device__ __forceinline__ void dequant_group_fp4(const uint4& wv, uint32_t S_blk0, uint32_t S_blk1,
                                                   uint32_t* out16) {
   const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t s2 = (i < 2) ? s2_blk0 : s2_blk1;
+    const uint32_t S = (i < 2) ? S_blk0 : S_blk1;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const uint32_t t = w4[i] >> (4 * m);
-      const uint32_t bits = ((t << 6) & 0x01C001C0u) | ((t << 12) & 0x80008000u);
-      uint32_t v;
-      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(bits), "r"(0x7E807E80u));   // 0x7E80 = bf16 2^126
-      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(v), "r"(s2));
+      // magnitude bits 4m..4m+2 of each half to 6..8, sign bit 4m+3 to 15
+      const uint32_t a = (m <= 1) ? (w4[i] << (6 - 4 * m)) : (w4[i] >> (4 * m - 6));
+      const uint32_t b = w4[i] << (12 - 4 * m);
+      uint32_t sel;
+      asm("lop3.b32 %0, %1, %2, %3, 0xE4;" : "=r"(sel) : "r"(a), "r"(b), "r"(0x01C001C0u));   // a where c, else b
+      const uint32_t bits = sel & 0x81C081C0u;
+      asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(out16[4 * i + m]) : "r"(bits), "r"(S));
     }
   }
 }
 
-// E4M3 scale byte -> its exact value as bf16 in both halves of a register. The byte's exponent and
-// mantissa bits moved to bf16 bits 4..10 and its sign to bit 15 read as the scale times 2^-120
-// (subnormal scales too); a packed multiply by 2^120 makes it exact.
-__device__ __forceinline__ uint32_t e4m3_to_bf16x2(uint32_t b) {
+// E4M3 scale byte -> its value times 2^118 as bf16 in both halves of a register. The byte's
+// exponent and mantissa bits moved to bf16 bits 4..10 and its sign to bit 15 read as the scale
+// times 2^-120 (subnormal scales too); packed multiplies by 2^127 and 2^111 are exact (the largest
+// scale, 448, becomes 1.75 * 2^126).
+__device__ __forceinline__ uint32_t fp4_block_scale(uint32_t b) {
   const uint32_t h = ((b & 0x7Fu) << 4) | ((b & 0x80u) << 8);
-  uint32_t v;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(__byte_perm(h, 0, 0x1010)), "r"(0x7B807B80u));   // 0x7B80 = bf16 2^120
-  return v;
+  uint32_t v, S;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(v) : "r"(__byte_perm(h, 0, 0x1010)), "r"(0x7F007F00u));   // bf16 2^127
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(S) : "r"(v), "r"(0x77007700u));                            // bf16 2^111
+  return S;
 }
+
+// The factor the fp4 epilogue applies to the fp32 sums: the matrix scale times 2^8 (see above).
+__device__ __forceinline__ float fp4_sum_scale(float gscale) { return gscale * 256.0f; }
 
 // Dequantise chunk c (0..7) of a stage row in the weight format FMT; sw4: the row's 16 scale bytes of
 // the stage (int4: eight bf16 scales, one per chunk; fp4: sixteen E4M3 scales, two per chunk).
@@ -248,7 +258,7 @@ template <int FMT, bool FAST = false>
 __device__ __forceinline__ void dequant_chunk(const uint4& wv, const uint32_t (&sw4)[4], int c, uint32_t* out16) {
   if (FMT == WFMT_FP4) {
     const uint32_t pair = (sw4[c >> 1] >> ((c & 1) * 16)) & 0xFFFFu;   // scale bytes 2c, 2c + 1
-    dequant_group_fp4(wv, e4m3_to_bf16x2(pair & 0xFFu), e4m3_to_bf16x2(pair >> 8), out16);
+    dequant_group_fp4(wv, fp4_block_scale(pair & 0xFFu), fp4_block_scale(pair >> 8), out16);
   } else {
     // chunk c's scale is half c % 2 of word c / 2: one byte permute copies it into both halves
     // (4% faster down GEMMs and 5% faster gate/up at 32-token tiles than a shift or mask and a multiply)
