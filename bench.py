@@ -22,6 +22,7 @@ import re
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -140,26 +141,43 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid: str | None):
+    def __init__(self, uuid: str | None, interval_ms: int = 50):
         self.proc = None
         self.uuid = uuid
+        self.interval_ms = interval_ms
 
     def start(self):
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        """Start sampling and return once the first sample is in: nvidia-smi's start-up queries,
+        left to overlap the timed region, slowed the host-bank workload's steps (which read host
+        memory) by tens of ms."""
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+               str(self.interval_ms)]
         if self.uuid:
             cmd += ["-i", self.uuid]
+        self.lines = []
         try:
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+            return
+        self.reader = threading.Thread(target=lambda: self.lines.extend(self.proc.stdout), daemon=True)
+        self.reader.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 10.0 and self.proc.poll() is None:
+            time.sleep(0.01)
+        time.sleep(2 * self.interval_ms / 1000.0)
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         time.sleep(0.1)
         self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
+        try:
+            self.proc.wait(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=10)
+        out = "".join(self.lines)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
@@ -807,13 +825,14 @@ def run_offload(args):
     touched = int((np.diff(d_off.cpu().numpy()) > 0).sum())
     gu_b, dn_b = expert_bytes(s)
 
-    clocks = ClockSampler(None)
+    clocks = ClockSampler(None, args.clock_interval_ms)
     clocks.start()
     torch.cuda.synchronize(dev)
     n0 = B.moe_launch_count()
-    # Each step is synchronised before the next is queued: queued back to back, the steps of
-    # this host-memory-bound workload took anywhere from 35.6 to 96 ms (the synchronised step
-    # 35.6-35.8 ms every time), so the back-to-back figure is reported beside it, not as the value.
+    # Each step is synchronised before the next is queued, and the same steps queued back to back
+    # are timed after it (reported beside the value). Both read the bank from host memory, and both
+    # have varied between runs (35.6 ms to about 120 ms a step), while the end-to-end loop measured
+    # later in the same runs held at 35.7-35.8 ms.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -921,6 +940,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-interval-ms", type=int, default=50,
+                    help="nvidia-smi sampling interval during the timed region of the host-bank workload")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
