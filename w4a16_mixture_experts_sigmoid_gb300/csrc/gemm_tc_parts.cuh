@@ -154,11 +154,14 @@ __device__ __forceinline__ void iss_commit_pair(uint64_t* bar, uint16_t mask) {
 // exact forms; both round the exact product q*s once to nearest even, so they
 // agree bit for bit (up to the sign of a zero product):
 // * FAST, for 2^-126 <= |s| < 2^-5 (exponent field 1..121, which holds for
-//   every practical int4 group scale): a nibble n masked into a zero exponent
-//   field reads as the bf16 subnormal n * 2^-133, and one packed fma with
-//   S = s * 2^133 (133 added to s's exponent field, still a normal bf16) and
-//   C = -8 s (exact) gives n*s - 8s = q*s, computed exactly and rounded once:
-//   an AND (plus the shift) and an fma a pair.
+//   every practical int4 group scale): bits 0..7 of a bf16 read as a linear
+//   field, b * 2^-133 for every b < 256 (the subnormals and the first normal
+//   binade), so a nibble n masked in place at bits 0..3 of a half is
+//   n * 2^-133 and at bits 4..7 is n * 2^-129. One packed fma with
+//   S = s * 2^133 or s * 2^129 (133 or 129 added to s's exponent field, still
+//   a normal bf16) and C = -8 s (exact) gives n*s - 8s = q*s, computed exactly
+//   and rounded once. Nibbles m and m+1 of a word need no shift between them:
+//   one shift by 8 per word, an AND and an fma a pair.
 // * otherwise (any scale): one lop3 makes the bf16 pattern 0x43<nibble> =
 //   128 + n exactly, one packed subtract of 136 gives q exactly, one packed
 //   multiply rounds q*s once: a lop3, a subtract and a multiply a pair.
@@ -170,15 +173,19 @@ template <bool FAST>
 __device__ __forceinline__ void dequant_group(const uint4& wv, uint32_t s2, uint32_t* out16) {
   const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
   if (FAST) {
-    const uint32_t S2 = s2 + 0x42804280u;   // exponent field + 133 in both halves (no carry: <= 254)
+    const uint32_t S0 = s2 + 0x42804280u;   // exponent field + 133 in both halves (no carry: <= 254)
+    const uint32_t S1 = s2 + 0x40804080u;   // exponent field + 129
     uint32_t C2;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(C2) : "r"(s2), "r"(0xC100C100u));   // 0xC100 = bf16 -8
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const uint32_t t = (w4[i] >> (4 * m)) & 0x000F000Fu;   // n * 2^-133 in each half
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out16[4 * i + m]) : "r"(t), "r"(S2), "r"(C2));
+        // nibbles m (low half) and m + 4 (high half): m even at bits 0..3 of each half of the word
+        // (m = 2 after a shift by 8), m odd at bits 4..7
+        const uint32_t src = (m < 2) ? w4[i] : (w4[i] >> 8);
+        const uint32_t t = src & ((m & 1) ? 0x00F000F0u : 0x000F000Fu);
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(out16[4 * i + m]) : "r"(t), "r"((m & 1) ? S1 : S0), "r"(C2));
       }
     }
   } else {
