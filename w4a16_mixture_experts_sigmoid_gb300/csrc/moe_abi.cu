@@ -23,8 +23,10 @@ using namespace moe;
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxDim = 32768;                  // H, I, shared_I
-constexpr int kSplitMaxT = 256;                 // the shared expert splits K for T up to this
-constexpr int kMaxSplit = 8;                    // K slices at most
+constexpr int kSplitMaxT = 256;                 // the shared expert and the router split K for T up to this
+constexpr int kMaxSplit = 32;                   // K slices at most
+constexpr int kSplitRows = 2048;                // K slices x T at most (bounds the fp32 partial sums)
+constexpr double kBf16StageBytes = 128.0 * 256 * 2;   // weight bytes of one K stage of a bf16 tile
 
 struct DevInfo {
   int sms = 0;
@@ -115,9 +117,15 @@ LayerW layer_w(const moe_weights_fp4_t* w) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// fp32 partial sums of a K-split bf16 GEMM with `rows` output rows of `cols` columns
+// The most K slices a T-token bf16 launch may take; the partial-sum buffers are sized for it.
+int max_split(int32_t T) {
+  if (T > kSplitMaxT) return 1;
+  return std::max(1, std::min(kMaxSplit, kSplitRows / std::max(T, 1)));
+}
+
+// fp32 partial sums of a K-split bf16 GEMM with T output rows of `cols` columns
 size_t split_part_bytes(int32_t T, int64_t cols) {
-  return T <= kSplitMaxT ? static_cast<size_t>(kMaxSplit) * T * cols * 4 : 0;
+  return T <= kSplitMaxT ? static_cast<size_t>(max_split(T)) * T * cols * 4 : 0;
 }
 
 // Workspace layout of moe_forward (byte offsets, each 256-aligned). With the router projection
@@ -148,7 +156,7 @@ Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I, bool project = f
   L.ys = take(shared_I > 0 ? static_cast<size_t>(T) * d.H * 4 : 0);
   // fp32 partial sums of the shared expert's K slices (small batches only)
   L.part_bytes = shared_I > 0 && T <= kSplitMaxT
-                     ? static_cast<size_t>(kMaxSplit) * T * std::max(2 * shared_I, d.H) * 4 : 0;
+                     ? static_cast<size_t>(max_split(T)) * T * std::max(2 * shared_I, d.H) * 4 : 0;
   L.part = take(L.part_bytes);
   L.logits = take(project ? static_cast<size_t>(T) * d.E * 4 : 0);
   L.rpart_bytes = project ? split_part_bytes(T, d.E) : 0;
@@ -157,15 +165,33 @@ Layout layout(const moe_dims_t& d, int32_t T, int32_t shared_I, bool project = f
   return L;
 }
 
-// K slices for a launch with `tiles` tiles: the fewest that give every SM a tile, dividing the
-// `stages` of the K loop, at most kMaxSplit; 1 when the tiles already cover the SMs.
-int pick_ksplit(int64_t tiles, int stages, int sms) {
+// K slices for a bf16 launch of `tiles` tiles over a K loop of `stages` stages, at T tokens, whose
+// slices each write `slice_bytes` of fp32 partial sums (read back once by the finishing kernel);
+// 1 when the tiles already cover the SMs. A slice count divides the stages and is at most
+// max_split(T). Where some count gives every SM a tile, the counts that do are weighed by an
+// estimate of the launch's time, in bytes at the whole GPU's rate: the busiest SM's stages x a
+// stage's weight bytes x the SMs (every SM streams at about the same rate), plus the partial sums
+// written and read; the least wins, ties going to fewer slices. Otherwise the most slices allowed.
+int pick_ksplit(int64_t tiles, int stages, int sms, int32_t T, double slice_bytes) {
   if (tiles >= sms) return 1;
-  int best = 1;
-  for (int d = 2; d <= kMaxSplit && d <= stages; ++d) {
+  const int most = std::min(max_split(T), stages);
+  int first = 0, last = 1;   // the fewest slices that cover the SMs; the most allowed
+  for (int d = 2; d <= most; ++d) {
     if (stages % d) continue;
-    best = d;
-    if (tiles * d >= sms) break;
+    last = d;
+    if (first == 0 && tiles * d >= sms) first = d;
+  }
+  if (first == 0) return last;
+  int best = first;
+  double best_cost = 0.0;
+  for (int d = first; d <= most; ++d) {
+    if (stages % d) continue;
+    const int64_t per_sm = (tiles * d + sms - 1) / sms;
+    const double cost = static_cast<double>(per_sm * (stages / d)) * kBf16StageBytes * sms + 2.0 * d * slice_bytes;
+    if (d == first || cost < best_cost) {
+      best = d;
+      best_cost = cost;
+    }
   }
   return best;
 }
@@ -299,7 +325,7 @@ moe_status_t run_shared(const moe_dims_t& d, const LayerW& w, const uint16_t* x,
   const bool split = part != nullptr && T <= kSplitMaxT && !(flags & MOE_FLAG_GEMM_SIMT);
   const int64_t chunks = (T + nt - 1) / nt;
   if (split) {
-    p.ksplit = pick_ksplit(chunks * (Is / 64), (d.H + 255) / 256, sms);
+    p.ksplit = pick_ksplit(chunks * (Is / 64), (d.H + 255) / 256, sms, T, static_cast<double>(T) * 2 * Is * 4);
     p.partial = part;
   }
   cudaError_t e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
@@ -314,7 +340,7 @@ moe_status_t run_shared(const moe_dims_t& d, const LayerW& w, const uint16_t* x,
   p.K = Is;
   p.rows_per_expert = d.H;
   p.out_cols = d.H;
-  if (split) p.ksplit = pick_ksplit(chunks * ((d.H + 127) / 128), (Is + 255) / 256, sms);
+  if (split) p.ksplit = pick_ksplit(chunks * ((d.H + 127) / 128), (Is + 255) / 256, sms, T, static_cast<double>(T) * d.H * 4);
   e = (flags & MOE_FLAG_GEMM_SIMT) ? launch_gemm_simt(p, s) : launch_gemm_tc(p, A_SMEM_BF16, nt, sms, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? MOE_ERR_UNSUPPORTED_SHAPE : MOE_ERR_CUDA;
   return MOE_OK;
@@ -346,7 +372,7 @@ moe_status_t run_router(const uint16_t* x, const uint16_t* wg, int32_t T, int32_
   const int nt = T <= 16 ? 16 : (T <= 32 ? 32 : 64);
   if (part != nullptr && T <= kSplitMaxT && !(flags & MOE_FLAG_GEMM_SIMT)) {
     const int64_t chunks = (T + nt - 1) / nt;
-    p.ksplit = pick_ksplit(chunks * ((E + 127) / 128), (H + 255) / 256, sms);
+    p.ksplit = pick_ksplit(chunks * ((E + 127) / 128), (H + 255) / 256, sms, T, static_cast<double>(T) * E * 4);
     p.partial = part;
   }
   const cudaError_t e =
