@@ -36,7 +36,9 @@ def run_permute(B, ids: np.ndarray, E: int, H: int = 64, gather: bool = True):
 
 @pytest.mark.parametrize("T,E,k,skew", [(16, 8, 2, None), (64, 384, 8, None), (4096, 384, 8, None),
                                         (1, 1, 1, None), (1000, 5, 3, None), (700, 64, 8, "one"),
-                                        (5000, 1024, 2, None), (333, 33, 7, "half")])
+                                        (5000, 1024, 2, None), (333, 33, 7, "half"),
+                                        (512, 1024, 8, None),     # 4096 assignments: the one-block path's largest
+                                        (513, 384, 8, "one")])    # 4104: two segments
 def test_permute_bit_exact(cuda_lib, T, E, k, skew):
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
     rng = np.random.default_rng(T * 7 + E)

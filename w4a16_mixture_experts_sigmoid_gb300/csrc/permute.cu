@@ -10,6 +10,9 @@
 //   scatter (one block per segment): per-warp histograms and bases, then each
 //           warp walks its slice (an eighth of the segment) 32 assignments at a
 //           time in order, ranking equal ids with __match_any_sync.
+// When the assignments fit one segment (small batches) one block does all three
+// in the same order, without the launches between them; the results are the
+// same.
 #include "common.cuh"
 #include "internal.h"
 
@@ -82,6 +85,34 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* __restrict__ hist, 
   if (e == E - 1) offsets[E] = excl + v;
 }
 
+// Walks warp `warp`'s slice [lo, hi) of the assignments 32 at a time in order and places each
+// valid one at its expert's running base in `mybase` (this warp's row of bases), ranking equal ids
+// within the 32 with __match_any_sync; an out-of-range id gets inv = -1.
+__device__ __forceinline__ void scatter_slice(const int32_t* __restrict__ ids, int64_t lo, int64_t hi, int k, int E,
+                                              int32_t* mybase, int32_t* __restrict__ sorted_ids,
+                                              int32_t* __restrict__ inv) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t i0 = lo; i0 < hi; i0 += 32) {
+    const int64_t i = i0 + lane;
+    int e = (i < hi) ? ids[i] : -1;
+    const bool ok = (e >= 0 && e < E);
+    if (!ok) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int32_t pos = 0;
+    if (ok) pos = mybase[e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) mybase[e] += __popc(peers);
+    __syncwarp();
+    if (ok) {
+      sorted_ids[pos] = static_cast<int32_t>(i / k);
+      inv[i] = pos;
+    } else if (i < hi) {
+      inv[i] = -1;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32_t* __restrict__ ids, int64_t Tk,
                                                                      int k, int E,
                                                                      const int32_t* __restrict__ hist,
@@ -115,26 +146,65 @@ __global__ void __launch_bounds__(kScatterWarps * 32) scatter_kernel(const int32
     }
   }
   __syncthreads();
-  int32_t* mybase = wb + warp * E;
-  for (int64_t i0 = lo; i0 < hi; i0 += 32) {
-    const int64_t i = i0 + lane;
-    int e = (i < hi) ? ids[i] : -1;
-    const bool ok = (e >= 0 && e < E);
-    if (!ok) e = -1;
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int32_t pos = 0;
-    if (ok) pos = mybase[e] + rank;
-    __syncwarp();
-    if (ok && rank == 0) mybase[e] += __popc(peers);
-    __syncwarp();
-    if (ok) {
-      sorted_ids[pos] = static_cast<int32_t>(i / k);
-      inv[i] = pos;
-    } else if (i < hi) {
-      inv[i] = -1;
+  scatter_slice(ids, lo, hi, k, E, wb + warp * E, sorted_ids, inv);
+}
+
+// count, scan and scatter in one block, for 1 <= Tk <= kSeg. The warps' slices, the per-warp bases
+// and the walk are the scatter kernel's for segment 0 (whose bases over earlier segments are 0), so
+// every output equals the three-kernel path's.
+__global__ void __launch_bounds__(kScatterWarps * 32) permute_one_block_kernel(const int32_t* __restrict__ ids, int Tk,
+                                                                               int k, int E,
+                                                                               int32_t* __restrict__ offsets,
+                                                                               int32_t* __restrict__ sorted_ids,
+                                                                               int32_t* __restrict__ inv,
+                                                                               int* status) {
+  griddep_wait();    // the predecessor in the stream has finished and its writes are visible
+  griddep_launch();  // the successor may start its own prologue
+  extern __shared__ int32_t wb[];  // [kScatterWarps][E]: per-warp counts, then per-warp bases
+  __shared__ int32_t warp_sum[kScatterWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wb[i] = 0;
+  __syncthreads();
+  const int slice = ((Tk + kScatterWarps - 1) / kScatterWarps + 31) / 32 * 32;
+  const int lo = min(Tk, warp * slice);
+  const int hi = min(Tk, lo + slice);
+  bool bad = false;
+  for (int i = lo + lane; i < hi; i += 32) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&wb[warp * E + e], 1);
+    else bad = true;
+  }
+  if (bad) record_status(status, MOE_ERR_DEVICE_BOUNDS);
+  __syncthreads();
+  // thread t owns experts [t*per, t*per + per): their totals, a block-wide exclusive scan of the
+  // totals, then offsets and each warp's base for those experts
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int32_t mine = 0;
+  for (int e = e0; e < e1; ++e)
+    for (int w = 0; w < kScatterWarps; ++w) mine += wb[w * E + e];
+  int32_t incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) warp_sum[warp] = incl;
+  __syncthreads();
+  int32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_sum[w];
+  int32_t base = before + incl - mine;
+  for (int e = e0; e < e1; ++e) {
+    offsets[e] = base;
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int32_t c = wb[w * E + e];
+      wb[w * E + e] = base;
+      base += c;
     }
   }
+  if (threadIdx.x == blockDim.x - 1) offsets[E] = before + incl;
+  __syncthreads();
+  scatter_slice(ids, lo, hi, k, E, wb + warp * E, sorted_ids, inv);
 }
 
 // Eight bf16 inputs (one 16-byte chunk) from natural order to the tensor-core
@@ -178,6 +248,12 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* off
                            int32_t* inv_perm, int32_t* hist, int* status, cudaStream_t s) {
   const int64_t Tk = (int64_t)T * k;
   const int nblk = permute_blocks(Tk);
+  if (nblk == 1) {
+    (void)launch_pdl(permute_one_block_kernel, dim3(1), dim3(kScatterWarps * 32), sizeof(int32_t) * kScatterWarps * E, s,
+                     ids, static_cast<int>(Tk), k, E, offsets, sorted_ids, inv_perm, status);
+    count_launches(1);
+    return cudaGetLastError();
+  }
   (void)launch_pdl(count_kernel, dim3(nblk), dim3(256), sizeof(int32_t) * E, s, ids, Tk, E, hist, status);
   (void)launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, s, hist, nblk, E, offsets);
   (void)launch_pdl(scatter_kernel, dim3(nblk), dim3(kScatterWarps * 32), sizeof(int32_t) * kScatterWarps * E, s, ids, Tk, k, E, hist, offsets,
