@@ -67,14 +67,23 @@ def test_unsupported_tile_size_is_rejected(cuda_lib):
         assert e.value.code == B.MOE_ERR_UNSUPPORTED_SHAPE
 
 
+CHAIN_CASES = [(33, 5, 288, 96, 37),
+               (33, 5, 288, 96, 1),      # one token
+               (33, 5, 288, 96, 3),
+               (384, 8, 256, 128, 2),    # the full expert count and top-k
+               (384, 8, 256, 128, 8),
+               (1024, 8, 256, 128, 3)]   # E = 1024: the widest routing registers
+
+
+@pytest.mark.parametrize("case", CHAIN_CASES, ids=[f"E{c[0]}k{c[1]}T{c[4]}" for c in CHAIN_CASES])
 @pytest.mark.parametrize("simt", [False, True])
-def test_split_calls_in_mma_order_chain_like_forward(cuda_lib, simt):
+def test_split_calls_in_mma_order_chain_like_forward(cuda_lib, simt, case):
     """route -> permute -> gate/up -> down (fp32 rows) -> combine with the tensor-core K order
     for the exchanged rows gives exactly the bits of moe_forward."""
     import torch
     from w4a16_mixture_experts_sigmoid_gb300 import binding as B
     from w4a16_mixture_experts_sigmoid_gb300.layer import MoeW4A16Layer
-    E, k, H, I, T = 33, 5, 288, 96, 37
+    E, k, H, I, T = case
     shape = synth.LayerShape(E=E, top_k=k, H=H, I=I)
     arrays = synth.make_layer(shape, seed=3)
     x, logits = synth.make_tokens(T, H, E, seed=4)

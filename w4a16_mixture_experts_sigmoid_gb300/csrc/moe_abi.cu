@@ -451,8 +451,11 @@ moe_status_t forward_device(const moe_dims_t& d, const LayerW& w, const uint16_t
   if (e == cudaSuccess && stage != nullptr)   // the touched experts, host bank -> device bank
     e = launch_stage_experts(stage->src, stage->dst, stage->bytes, offsets, d.E, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // The layer's kernels before the GEMMs began with route's wait, so a resident bank and the offsets
-  // are complete when the GEMMs start; a bank staged by this call is not (it is the predecessor's output).
+  // A GEMM with weights_ready reads the bank and the offsets without waiting for its predecessor.
+  // The offsets are complete by then because the gather kernel sits between the permutation and
+  // the GEMM: it waits for the permutation to finish before it lets the GEMM launch. (A kernel that
+  // wrote the offsets and then let the GEMM launch directly would race with it.) A bank staged by
+  // this call is the predecessor's own output, so those GEMMs wait.
   const bool ready = stage == nullptr;
   moe_status_t st = run_grouped_gemm(MOE_GEMM_GATEUP_SILU, d, w, xperm, T, offsets, h, status, flags, mma_order,
                                      nullptr, sms, s, ready);
